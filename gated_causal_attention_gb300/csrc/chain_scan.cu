@@ -1,0 +1,341 @@
+// chain_scan.cu -- single-pass chunked forward substitution of (I - A) y = b (K3).
+//
+// "Resolvent Operator", section "The path-product corner is a resolvent": the readout at
+// (beta, qk, g) = (0, 0, 1) is the chain y_i = a_i y_{i-1} + b_i, i.e. forward substitution
+// of (I - A) y = b with A the gate shift. Here y_0 = b_0 (the page's y_0 = 0 is b_0 = 0).
+//
+// Each CTA takes a ticket (an atomic counter, so tickets follow the order CTAs start in)
+// and owns one chunk of 128 tokens x dv channels of one head:
+//   1. the chunk of b arrives in shared memory by one bulk copy; the gates are formed;
+//   2. each of 8 warps runs the recurrence over its 16 tokens from a zero carry and keeps
+//      the affine map (A_w, Y_w) of its stretch: y_out = A_w y_in + Y_w;
+//   3. warp 0 composes the 8 maps into the chunk's map and publishes it; then looks back
+//      over earlier chunks of the same head (their maps, or the carry a chunk already
+//      resolved) until it knows y at the end of the previous chunk, and publishes its own
+//      resolved carry. A map with A = 0 (a closed gate) ends the look-back early;
+//   4. every warp reruns its stretch from the true carry and writes y.
+// b is read once and y written once. Every wait on another chunk is bounded in time and
+// sets RS_STATUS_TIMEOUT (carry taken as 0) when it runs out, so the kernel always ends.
+#include "common.cuh"
+
+namespace rs {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kTokPerWarp = kChainChunk / kWarps;  // 16
+
+template <typename BT>
+__device__ __forceinline__ float load_val(const BT *p);
+template <>
+__device__ __forceinline__ float load_val<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float load_val<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(*p);
+}
+
+template <int CPL, typename BT>
+__global__ void __launch_bounds__(256)
+chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_ticket;
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ cplx s_gate[kChainChunk];
+    __shared__ cplx s_warpA[kWarps], s_exA[kWarps];
+
+    const int dv = a.dv, n = a.n;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nchunks = (n + kChainChunk - 1) / kChainChunk;
+
+    BT *sb = reinterpret_cast<BT *>(smem);                                     // [128][dv]
+    cplx *s_warpY = reinterpret_cast<cplx *>(smem + sizeof(BT) * kChainChunk * dv);  // [8][dv]
+    cplx *s_exY = s_warpY + kWarps * dv;                                        // [8][dv]
+    cplx *s_yin = s_exY + kWarps * dv;                                          // [dv]
+
+    if (tid == 0) {
+        s_ticket = atomicAdd(a.counter, 1);
+        mbar_init(&s_bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int ticket = s_ticket;
+    const int slot = ticket / nchunks, chunk = ticket % nchunks;
+    if (slot >= tab.count) return;
+    const int64_t bh = tab.bh[slot];
+    const float g = tab.g[slot];
+    const int s0 = chunk * kChainChunk;
+    const int len = min(kChainChunk, n - s0);
+    const BT *bsrc = reinterpret_cast<const BT *>(a.b) + (bh * n + s0) * (int64_t)dv;
+    const uint32_t bytes = (uint32_t)(len * dv * sizeof(BT));
+    const bool bulk = (bytes % 16u) == 0 && (reinterpret_cast<uintptr_t>(bsrc) % 16u) == 0;
+
+    if (bulk) {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&s_bar, bytes);
+            bulk_load(sb, bsrc, bytes, &s_bar);
+        }
+    } else {
+        for (int e = tid; e < len * dv; e += blockDim.x) sb[e] = bsrc[e];
+    }
+
+    // gates of this chunk ("Object": blended gate and gate)
+    bool bad = false;
+    if (tid < kChainChunk) {
+        const int t = s0 + tid;
+        cplx at = {1.f, 0.f};
+        if (tid < len) {
+            const float uu = a.u[bh * n + t], th = a.theta[bh * n + t];
+            const float m = fminf(fmaxf(fmaf(g, uu, 1.f - g), 0.f), 1.f);
+            const float tp = g * th;
+            bad = !isfinite(uu) || !isfinite(th) || !isfinite(tp);
+            float sn, cs;
+            sincosf(tp, &sn, &cs);
+            at = {m * cs, m * sn};
+            if (t == 0) at = {0.f, 0.f};  // y_0 = b_0: nothing flows in ahead of token 0
+        }
+        s_gate[tid] = at;
+    }
+    if (__syncthreads_or(bad) && tid == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
+    __shared__ int s_loaded;
+    if (tid == 0) {
+        s_loaded = !bulk || mbar_wait(&s_bar, 0, a.wait_limit_ns);
+        if (!s_loaded) flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
+    }
+    __syncthreads();
+    if (!s_loaded) return;  // the chunk never arrived: give up on it (uniform across the CTA)
+
+    const int ch0 = lane * CPL;
+    const int tok0 = warp * kTokPerWarp;
+    const int tok1 = min(tok0 + kTokPerWarp, len);
+
+    // pass 1: each warp's stretch as an affine map from a zero carry
+    {
+        cplx y[CPL];
+        cplx A = {1.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) y[c] = {0.f, 0.f};
+        for (int t = tok0; t < tok1; ++t) {
+            const cplx at = s_gate[t];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const float bv = (ch0 + c < dv) ? load_val(sb + t * dv + ch0 + c) : 0.f;
+                y[c] = cmul(at, y[c]);
+                y[c].re += bv;
+            }
+            A = cmul(at, A);
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (ch0 + c < dv) s_warpY[warp * dv + ch0 + c] = y[c];
+        if (lane == 0) s_warpA[warp] = A;
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // compose the warps' maps: exclusive prefixes and the chunk's map
+        cplx eA = {1.f, 0.f};
+        cplx eY[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) eY[c] = {0.f, 0.f};
+        for (int w = 0; w < kWarps; ++w) {
+            if (lane == 0) s_exA[w] = eA;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                if (ch0 + c < dv) s_exY[w * dv + ch0 + c] = eY[c];
+            const cplx wA = s_warpA[w];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const cplx wY = (ch0 + c < dv) ? s_warpY[w * dv + ch0 + c] : cplx{0.f, 0.f};
+                const cplx t = cmul(wA, eY[c]);
+                eY[c] = {t.re + wY.re, t.im + wY.im};
+            }
+            eA = cmul(wA, eA);
+        }
+
+        const int64_t me = (int64_t)slot * nchunks + chunk;
+        const bool publish = ticket != a.withhold_chunk;
+        cplx yin[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) yin[c] = {0.f, 0.f};
+
+        if (chunk == 0) {
+            // nothing before the first chunk: its resolved carry is its own map's offset
+            if (publish) {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+                    if (ch0 + c < dv) a.incl_y[me * dv + ch0 + c] = make_float2(eY[c].re, eY[c].im);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(a.flags + me, 2);
+            }
+        } else {
+            if (publish) {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+                    if (ch0 + c < dv) a.agg_y[me * dv + ch0 + c] = make_float2(eY[c].re, eY[c].im);
+                if (lane == 0) a.agg_a[me] = make_float2(eA.re, eA.im);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(a.flags + me, 1);
+            }
+            // look back: acc maps y_end(p) to y_end(chunk-1)
+            cplx accA = {1.f, 0.f};
+            cplx accY[CPL];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) accY[c] = {0.f, 0.f};
+            for (int p = chunk - 1; p >= 0; --p) {
+                const int64_t other = (int64_t)slot * nchunks + p;
+                int f = 0;
+                if (lane == 0) {
+                    f = ld_acquire_gpu(a.flags + other);
+                    if (f == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while ((f = ld_acquire_gpu(a.flags + other)) == 0) {
+                            if (globaltimer_ns() - t0 > a.wait_limit_ns) break;
+                            __nanosleep(64);
+                        }
+                    }
+                }
+                f = __shfl_sync(0xffffffffu, f, 0);
+                __syncwarp();
+                __threadfence();
+                if (f == 0) {  // ran out of time: take the carry as 0 and say so
+                    if (lane == 0) flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) yin[c] = accY[c];
+                    break;
+                }
+                if (f == 2) {
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) {
+                        cplx yp = {0.f, 0.f};
+                        if (ch0 + c < dv) {
+                            const float2 v = __ldcg(a.incl_y + other * dv + ch0 + c);
+                            yp = {v.x, v.y};
+                        }
+                        const cplx t = cmul(accA, yp);
+                        yin[c] = {t.re + accY[c].re, t.im + accY[c].im};
+                    }
+                    break;
+                }
+                const float2 pa = __ldcg(a.agg_a + other);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    cplx yp = {0.f, 0.f};
+                    if (ch0 + c < dv) {
+                        const float2 v = __ldcg(a.agg_y + other * dv + ch0 + c);
+                        yp = {v.x, v.y};
+                    }
+                    const cplx t = cmul(accA, yp);
+                    accY[c] = {t.re + accY[c].re, t.im + accY[c].im};
+                }
+                accA = cmul(accA, {pa.x, pa.y});
+                if (!cnonzero(accA)) {  // a closed gate: nothing earlier reaches this chunk
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) yin[c] = accY[c];
+                    break;
+                }
+            }
+            if (publish) {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    const cplx t = cmul(eA, yin[c]);
+                    if (ch0 + c < dv)
+                        a.incl_y[me * dv + ch0 + c] =
+                            make_float2(t.re + eY[c].re, t.im + eY[c].im);
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(a.flags + me, 2);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (ch0 + c < dv) s_yin[ch0 + c] = yin[c];
+    }
+    __syncthreads();
+
+    // pass 2: rerun each stretch from its true carry and write y
+    {
+        const cplx wA = s_exA[warp];
+        cplx y[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            if (ch0 + c < dv) {
+                const cplx t = cmul(wA, s_yin[ch0 + c]);
+                const cplx e = s_exY[warp * dv + ch0 + c];
+                y[c] = {t.re + e.re, t.im + e.im};
+            } else {
+                y[c] = {0.f, 0.f};
+            }
+        }
+        float *yr = a.y_re + (bh * n + s0) * (int64_t)dv;
+        float *yi = a.y_im + (bh * n + s0) * (int64_t)dv;
+        for (int t = tok0; t < tok1; ++t) {
+            const cplx at = s_gate[t];
+            float vr[CPL], vi[CPL];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const float bv = (ch0 + c < dv) ? load_val(sb + t * dv + ch0 + c) : 0.f;
+                y[c] = cmul(at, y[c]);
+                y[c].re += bv;
+                vr[c] = y[c].re;
+                vi[c] = y[c].im;
+            }
+            if (ch0 + CPL <= dv && (dv % CPL) == 0) {
+                if constexpr (CPL == 4) {
+                    *reinterpret_cast<float4 *>(yr + t * dv + ch0) = make_float4(vr[0], vr[1], vr[2], vr[3]);
+                    *reinterpret_cast<float4 *>(yi + t * dv + ch0) = make_float4(vi[0], vi[1], vi[2], vi[3]);
+                } else if constexpr (CPL == 2) {
+                    *reinterpret_cast<float2 *>(yr + t * dv + ch0) = make_float2(vr[0], vr[1]);
+                    *reinterpret_cast<float2 *>(yi + t * dv + ch0) = make_float2(vi[0], vi[1]);
+                } else {
+                    yr[t * dv + ch0] = vr[0];
+                    yi[t * dv + ch0] = vi[0];
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+                    if (ch0 + c < dv) {
+                        yr[t * dv + ch0 + c] = vr[c];
+                        yi[t * dv + ch0 + c] = vi[c];
+                    }
+            }
+        }
+    }
+}
+
+template <int CPL, typename BT>
+cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
+{
+    const int nchunks = (a.n + kChainChunk - 1) / kChainChunk;
+    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (2 * kWarps + 1) * a.dv;
+    auto k = chain_scan_kernel<CPL, BT>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<tab.count * nchunks, 256, smem, s>>>(a, tab);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chain_scratch_bytes(int slots, int n, int dv)
+{
+    const size_t nchunks = (size_t)(n + kChainChunk - 1) / kChainChunk;
+    const size_t chunks = (size_t)slots * nchunks;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    return up(sizeof(int) * (chunks + 1)) + up(sizeof(float2) * chunks) +
+           2 * up(sizeof(float2) * chunks * (size_t)dv);
+}
+
+cudaError_t launch_chain_scan(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
+{
+    if (tab.count == 0 || a.n == 0) return cudaSuccess;
+    if (a.dv <= 32) return a.b_is_bf16 ? launch_t<1, __nv_bfloat16>(a, tab, s) : launch_t<1, float>(a, tab, s);
+    if (a.dv <= 64) return a.b_is_bf16 ? launch_t<2, __nv_bfloat16>(a, tab, s) : launch_t<2, float>(a, tab, s);
+    return a.b_is_bf16 ? launch_t<4, __nv_bfloat16>(a, tab, s) : launch_t<4, float>(a, tab, s);
+}
+
+}  // namespace rs

@@ -1,0 +1,88 @@
+// resolvent_internal.h -- launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+namespace rs {
+
+constexpr int kBlock = 128;          // token block = key/query tile of the head kernel
+constexpr int kMaxSlots = 128;       // heads per launch (the head table travels as a kernel parameter)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any device-side wait: 2 s
+constexpr int32_t RS_STATUS_NONFINITE_BIT = 0x1;  // same values as the public RS_STATUS_* bits
+constexpr int32_t RS_STATUS_TIMEOUT_BIT = 0x2;
+
+// Heads handled by one launch: slot -> (b*H + h, switches). Passed by value.
+struct HeadTable {
+    int count;
+    int bh[kMaxSlots];
+    float beta[kMaxSlots];
+    float qk[kMaxSlots];
+    float g[kMaxSlots];
+};
+
+// ---------------------------------------------------------------- gate preparation (K1)
+struct GatePrepArgs {
+    const float *u, *theta;
+    int n;
+    float *m, *theta_p;          // [BH,n] or null
+    float2 *gate, *prefix, *suffix;  // [BH,n] or null
+    float2 *carry;               // [BH,nb] or null
+    int32_t *status;
+    int write_ungated;           // 0: heads with g == 0 are only checked (nothing written)
+};
+cudaError_t launch_gate_prep(const GatePrepArgs &a, const HeadTable &tab, cudaStream_t s);
+
+// ---------------------------------------------------------------- finiteness / conversion
+cudaError_t launch_check_finite_bf16(const __nv_bfloat16 *x, int64_t per_head, const HeadTable &tab,
+                                     int32_t *status, cudaStream_t s);
+cudaError_t launch_check_finite_f32(const float *x, int64_t per_head, const HeadTable &tab,
+                                    int32_t *status, cudaStream_t s);
+// Rows of `cols` values (fp32 or bf16) -> rows of `dst_cols` bf16 (round to nearest even),
+// zero-padded on the right. check_finite: flag non-finite source values.
+cudaError_t launch_pad_to_bf16(const void *src, int src_is_f32, int64_t rows, int cols,
+                               __nv_bfloat16 *dst, int dst_cols, int32_t *status,
+                               int check_finite, cudaStream_t s);
+
+// ---------------------------------------------------------------- chain scan (K3)
+struct ChainArgs {
+    const float *u, *theta;
+    const void *b;               // fp32 or bf16 [BH,n,dv]
+    int b_is_bf16;
+    int n, dv;
+    float *y_re, *y_im;
+    int *counter;                // ticket counter (zeroed before launch)
+    int *flags;                  // [slots * nchunks] (zeroed before launch)
+    float2 *agg_a;               // [slots * nchunks]
+    float2 *agg_y;               // [slots * nchunks * dv]
+    float2 *incl_y;              // [slots * nchunks * dv]
+    int32_t *status;
+    uint64_t wait_limit_ns;
+    int withhold_chunk;          // test knob: this ticket never publishes (-1: none)
+};
+constexpr int kChainChunk = 128;
+size_t chain_scratch_bytes(int slots, int n, int dv);
+cudaError_t launch_chain_scan(const ChainArgs &a, const HeadTable &tab, cudaStream_t s);
+
+// ---------------------------------------------------------------- head kernel (K2)
+struct HeadArgs {
+    int n, d, dv;
+    const float2 *gate, *prefix, *suffix, *carry;  // gate products of K1 (gated heads)
+    float *O_re, *O_im;
+    int32_t *status;
+};
+// dpad, dvpad in {64, 128}
+cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
+                            const CUtensorMap &tk, const CUtensorMap &tv, int dpad, int dvpad,
+                            cudaStream_t s);
+
+// ---------------------------------------------------------------- debug path product
+cudaError_t launch_debug_path_product(const float2 *gate, const float2 *prefix,
+                                      const float2 *suffix, const float2 *carry, int n,
+                                      const HeadTable &tab, float2 *G, cudaStream_t s);
+
+}  // namespace rs

@@ -1,0 +1,179 @@
+/*
+ * resolvent.h -- C ABI of the GB300 (sm_103a) resolvent-operator causal head.
+ *
+ * The operation is the one causal attention head of "Resolvent Operator"
+ * (teerth.dev/Aether-Lang/integrated/resolvent/), section "Object": for 0 <= j <= i < n
+ *
+ *   s_ij = <q_i, k_j> / sqrt(d)                         scaled logit
+ *   m_k  = clamp(lerp(1, u_k, g), 0, 1),  theta'_k = g theta_k     blended gate
+ *   a_k  = m_k e^{i theta'_k}                            the gate
+ *   G_ij = prod_{k=j+1..i} a_k  (G_ii = 1),  R_ij = |G_ij|           path product, modulus
+ *   Z_i  = sum_{j<=i} R_ij e^{qk s_ij}                   row normaliser
+ *   W_ij = G_ij e^{qk s_ij} / Z_i^beta  (j <= i),  0 above           weight
+ *   O_i  = sum_{j<=i} W_ij V_j                           readout (complex; V real)
+ *
+ * evaluated in the log domain of section "Evaluation and refusals" (Z from a sum shifted by
+ * the maximum over live entries R_ij > 0), with the refusals of that section. The chain of
+ * section "The path-product corner is a resolvent" (y_i = a_i y_{i-1} + b_i) is the
+ * readout at the corner (beta, qk, g) = (0, 0, 1).
+ *
+ * Conventions shared by every entry point
+ *  - Device pointers unless stated otherwise; the caller owns every buffer. The library
+ *    never allocates or frees memory and never synchronises, except in
+ *    resolvent_status_sync. Scratch lives in the caller's workspace.
+ *  - Layout: row-major and contiguous. A head is one (batch, head) slice bh = b*H + h:
+ *    q, k [B,H,n,d]; v, b [B,H,n,dv]; u, theta [B,H,n]; O_re, O_im, y_re, y_im [B,H,n,dv].
+ *    Complex per-token arrays (gate, prefix, suffix, block carry) hold interleaved
+ *    (re, im) fp32 pairs.
+ *  - Alignment: every pointer 16-byte aligned; head_forward also needs d % 8 == 0.
+ *  - Switches (rs_switches) are HOST arrays of `count` values, count 1 (all heads) or H
+ *    (value h serves head h of every batch). Non-finite switches are refused at once.
+ *  - Errors found from arguments are returned synchronously. Errors that depend on the
+ *    data (the pages' NonFinite refusal; a bounded wait that ran out) are OR-ed into the
+ *    caller's device status word `status_dev` (one int32, zero before the first call) and
+ *    read back by resolvent_status_sync. Outputs are unspecified when a refusal is raised.
+ *  - n == 0 or B*H == 0 is an empty call: RS_OK, nothing launched ("Evaluation and
+ *    refusals", empty sequence).
+ *  - `stream` is a cudaStream_t (0 = the legacy default stream); every launch goes there.
+ */
+#ifndef RESOLVENT_H
+#define RESOLVENT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RS_OK = 0,
+    RS_ERR_NONFINITE = 1,   /* the pages' NonFinite: a non-finite input, switch, g*theta or logit */
+    RS_ERR_SHAPE = 2,       /* negative sizes, d = 0 or dv = 0 with n > 0, bad switch count */
+    RS_ERR_UNSUPPORTED = 3, /* a size this build does not handle (d or dv > 128, d % 8 != 0) */
+    RS_ERR_ALIGN = 4,       /* a pointer that is not 16-byte aligned */
+    RS_ERR_WORKSPACE = 5,   /* workspace missing or smaller than the *_workspace_bytes query */
+    RS_ERR_CUDA = 6,        /* a CUDA runtime call failed (launch, tensor map, memset) */
+    RS_ERR_TIMEOUT = 7      /* a bounded device-side wait ran out (reported via status_dev) */
+} rs_status;
+
+typedef enum { RS_F32 = 0, RS_BF16 = 1 } rs_dtype;
+
+/* Per-head switches (beta, qk, g) -- the Rust API's `Switches`. Host arrays. */
+typedef struct {
+    const float *beta;
+    const float *qk;
+    const float *g;
+    int count;
+} rs_switches;
+
+/* Device status-word bits (OR-ed by kernels). */
+#define RS_STATUS_NONFINITE 0x1
+#define RS_STATUS_TIMEOUT 0x2
+
+/* Token block of the gate products (the key/query tile of the head kernel). */
+#define RS_BLOCK 128
+
+/*
+ * Gate preparation ("Object", blended-gate and gate rows; Rust API `blend`, `gate`) and
+ * the block products that factor the path product ("Object", path-product row):
+ * for each head and each block [s, e] of RS_BLOCK tokens (the last one ragged)
+ *   m[t] = clamp((1-g) + g u_t, 0, 1),  theta_p[t] = g theta_t,  gate[t] = a_t
+ *   prefix[i] = prod_{k=max(s,1)..i} a_k       (inclusive, from the block's first token)
+ *   suffix[j] = prod_{k=j+1..e} a_k           (exclusive; 1 at j = e)
+ *   block_carry[b] = prod_{k=max(s,1)..e} a_k (the whole block)
+ * so that for j < s(QB) <= i the path product is
+ *   G_ij = prefix[i] * (prod of block_carry over the blocks strictly between) * suffix[j].
+ * Gates are only multiplied (never divided or taken through a log), so a closed gate gives
+ * exact zeros. a_0 is never read. Shapes: m, theta_p [B,H,n] fp32; gate, prefix, suffix
+ * [B,H,n] complex; block_carry [B,H,ceil(n/RS_BLOCK)] complex. Any output may be NULL.
+ * Non-finite u, theta, or an overflowing g*theta sets RS_STATUS_NONFINITE.
+ */
+rs_status resolvent_gate_prep(const float *u, const float *theta, rs_switches sw,
+                              int B, int H, int n,
+                              float *m, float *theta_p, float *gate, float *prefix,
+                              float *suffix, float *block_carry,
+                              int32_t *status_dev, void *stream);
+
+/* Workspace bytes resolvent_head_forward needs for these sizes (0 when n == 0). */
+size_t resolvent_head_workspace_bytes(int B, int H, int n, int d, int dv, rs_dtype dtype);
+
+/*
+ * The head: O = W V with W from section "Object" (Rust API `operator` then `readout`,
+ * fused, batched over B*H heads, per-head switches). q, k [B,H,n,d] and v [B,H,n,dv] are
+ * bf16 (dtype RS_BF16) or fp32 (RS_F32: rounded to bf16 into the workspace first);
+ * u, theta fp32 [B,H,n]; O_re, O_im fp32 [B,H,n,dv]. The contractions run on the tensor
+ * cores in bf16 with fp32 accumulation. Heads with qk = 0 and beta = 0 (W = G exactly)
+ * are evaluated as the chain. Supported: 1 <= d <= 128 with d % 8 == 0, 1 <= dv <= 128.
+ * Refusals (RS_STATUS_NONFINITE): non-finite q, k, u, theta, g*theta, or a non-finite
+ * logit qk*s_ij on an evaluated entry (every diagonal entry is evaluated, so any
+ * non-finite q or k row is caught). Outputs past the range of fp32 read +-inf, not NaN.
+ */
+rs_status resolvent_head_forward(const void *q, const void *k, const float *u,
+                                 const float *theta, const void *v, rs_switches sw,
+                                 int B, int H, int n, int d, int dv, rs_dtype dtype,
+                                 float *O_re, float *O_im,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *status_dev, void *stream);
+
+/* Workspace bytes resolvent_chain_scan needs for these sizes (0 when n == 0). */
+size_t resolvent_chain_workspace_bytes(int B, int H, int n, int dv);
+
+/*
+ * The chain of section "The path-product corner is a resolvent" (Rust API `chain_label`):
+ * y_0 = b_0, y_i = a_i y_{i-1} + b_i with a_i the gate of (u_i, theta_i, g) -- i.e. the
+ * readout G b of the path product. The page states it for b_0 = 0, where y_0 = 0.
+ * b fp32 [B,H,n,dv]; y_re, y_im fp32 [B,H,n,dv]; 1 <= dv <= 128. Only g is read from the
+ * switches (the chain is the (0,0,1) corner whatever beta and qk say).
+ * Single pass: chunks of tokens publish their carries to later chunks; every wait on a
+ * carry is bounded, and one that runs out sets RS_STATUS_TIMEOUT.
+ */
+rs_status resolvent_chain_scan(const float *u, const float *theta, rs_switches sw,
+                               const float *b, int B, int H, int n, int dv,
+                               float *y_re, float *y_im,
+                               void *workspace, size_t workspace_bytes,
+                               int32_t *status_dev, void *stream);
+
+/* Synchronises `stream`, reads the status word, clears it to 0 and returns RS_OK,
+ * RS_ERR_NONFINITE or RS_ERR_TIMEOUT (RS_ERR_CUDA if the runtime reports an error). */
+rs_status resolvent_status_sync(int32_t *status_dev, void *stream);
+
+/* Static text for a status code. */
+const char *resolvent_status_string(rs_status s);
+
+/* Number of kernel launches the last call on this host thread enqueued (for reporting). */
+int resolvent_last_launch_count(void);
+
+/*
+ * Debug export (tests only): the path product G [B,H,n,n] complex (interleaved) as the
+ * head kernel factors it -- prefix x block carries x suffix across blocks, explicit
+ * products inside a block -- from the gates of (u, theta, g). n <= 4096.
+ */
+rs_status resolvent_debug_path_product(const float *u, const float *theta, rs_switches sw,
+                                       int B, int H, int n, float *G,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *status_dev, void *stream);
+
+/*
+ * Test knobs (tests only; they change how later calls on any thread behave):
+ *  - the bound on device-side waits in the chain scan, in nanoseconds (0 restores 2 s);
+ *  - a chain chunk ticket that never publishes its carry (-1: none), so that the bounded
+ *    wait of the chunks after it runs out and RS_STATUS_TIMEOUT is raised without a hang.
+ */
+void resolvent_test_set_wait_limit_ns(uint64_t ns);
+void resolvent_test_set_chain_withhold(int ticket);
+
+/*
+ * Kernel timing (benchmarking): while enabled, each call records a pair of CUDA events on
+ * its stream around its main kernel -- the fused head kernel(s), or the chain scan when the
+ * call has no other heads. resolvent_profile_collect waits for the recorded pairs, writes
+ * their durations in milliseconds (at most `max`), returns how many, and starts a new
+ * series (-1 on a CUDA error). Enabling (re)starts the series. Up to 1024 pairs are kept.
+ */
+rs_status resolvent_profile_enable(int on);
+int resolvent_profile_collect(float *ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

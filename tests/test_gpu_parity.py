@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded
+inputs, plus invariants that need no oracle.
+
+Tolerances (the method's statement of the target): O within max-abs 1e-2 * max|O| per head
+(bf16 tensor-core contractions); gate products within 1e-5 relative (normwise for complex
+values); the chain within 1e-5 of its forward-error envelope; the zero pattern of G exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+GATE_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def R():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_causal_attention_gb300 as R
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    return R
+
+
+def dev(x, dtype=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dtype).cuda()
+
+
+def f32(xs):
+    """Switch values as the GPU sees them (fp32), widened for the oracle."""
+    return np.asarray(xs, dtype=np.float32).astype(np.float64)
+
+
+def run_head(R, hi: W.HeadInputs):
+    dt = torch.bfloat16 if hi.dtype == "bf16" else torch.float32
+    shp = (hi.B, hi.H, hi.n)
+    q = dev(hi.q.reshape(*shp, hi.d), dt)
+    k = dev(hi.k.reshape(*shp, hi.d), dt)
+    v = dev(hi.v.reshape(*shp, hi.dv), dt)
+    u = dev(hi.u.reshape(shp)); th = dev(hi.theta.reshape(shp))
+    Ore, Oim = R.head_forward(q, k, u, th, v, hi.beta, hi.qk, hi.g)
+    torch.cuda.synchronize()
+    O = (Ore.cpu().double().numpy() + 1j * Oim.cpu().double().numpy()).reshape(hi.B * hi.H, hi.n, hi.dv)
+    return O
+
+
+def oracle_rows(oracle_mod, hi: W.HeadInputs, rows):
+    beta, qk, g = [f32(x) for x in hi.switches_bh()]
+    O, st = oracle_mod.head_rows(hi.q, hi.k, hi.u, hi.theta, hi.v, beta, qk, g, rows)
+    assert np.all(st == 0)
+    return O
+
+
+def assert_head_close(O_gpu, O_ref, rows, what=""):
+    """Per head: max |O_gpu - O_ref| <= 1e-2 * max |O_ref| over both halves."""
+    worst = 0.0
+    for h in range(O_ref.shape[0]):
+        ref = O_ref[h]
+        got = O_gpu[h][rows]
+        scale = max(np.max(np.abs(ref.real)), np.max(np.abs(ref.imag)))
+        err = max(np.max(np.abs(got.real - ref.real)), np.max(np.abs(got.imag - ref.imag)))
+        assert np.all(np.isfinite(got)), f"{what} head {h}: non-finite output"
+        assert err <= O_TOL * scale, f"{what} head {h}: err {err:.3e} > {O_TOL} * {scale:.3e}"
+        worst = max(worst, err / max(scale, 1e-300))
+    return worst
+
+
+# ------------------------------------------------------------------ gate preparation
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 300, 1000])
+def test_gate_prep_matches_oracle(R, oracle_mod, n):
+    B, H = 2, 3
+    r = np.random.default_rng(100 + n)
+    u = r.uniform(-0.5, 1.5, (B * H, n)).astype(np.float32)
+    th = r.uniform(-math.pi, math.pi, (B * H, n)).astype(np.float32)
+    u[r.uniform(size=u.shape) < 0.03] = 0.0
+    gs = [0.0, 0.3, 1.0]
+    out = R.gate_prep(dev(u.reshape(B, H, n)), dev(th.reshape(B, H, n)), gs)
+    ref = oracle_mod.gate_prep(u, th, f32(np.tile(gs, B)), block=128)
+    assert np.all(ref["status"] == 0)
+    m = out["m"].cpu().double().numpy().reshape(B * H, n)
+    tp = out["theta_p"].cpu().double().numpy().reshape(B * H, n)
+    assert np.all(np.abs(m - ref["m"]) <= GATE_TOL * np.abs(ref["m"]) + 1e-30)
+    assert np.all(np.abs(tp - ref["theta_p"]) <= GATE_TOL * np.abs(ref["theta_p"]) + 1e-30)
+    for key in ("gate", "prefix", "suffix", "carry"):
+        got = torch.view_as_complex(out[key]).cpu().numpy().astype(np.complex128).reshape(B * H, -1)
+        want = ref[key]
+        big = np.abs(want) >= 1e-30
+        rel = np.abs(got - want)[big] / np.abs(want)[big]
+        assert rel.size == 0 or rel.max() <= GATE_TOL, f"{key}: {rel.max():.3e}"
+        # structural zeros are exact zeros; entries above fp32's normal range are nonzero
+        assert np.all(got[want == 0] == 0), key
+        assert np.all(got[np.abs(want) >= 2.0 ** -126] != 0), key
+
+
+def test_path_product_zero_pattern_is_exact(R, oracle_mod):
+    """Every structural zero of G (a closed gate on the path) is an exact 0 on the GPU, and
+    every entry of |G| >= 2^-126 is nonzero; values within 1e-5 normwise."""
+    B, H, n = 1, 3, 300
+    r = np.random.default_rng(7)
+    u = r.uniform(0.9, 1.0, (B * H, n)).astype(np.float32)
+    th = r.uniform(-math.pi, math.pi, (B * H, n)).astype(np.float32)
+    u[:, [5, 130, 131, 255, 256, 299]] = 0.0
+    gs = [1.0, 0.5, 1.0]
+    G = R.debug_path_product(dev(u.reshape(B, H, n)), dev(th.reshape(B, H, n)), gs)
+    G = G.cpu().numpy().astype(np.complex128).reshape(B * H, n, n)
+    gates = oracle_mod.gate_prep(u, th, f32(gs), block=128)["gate"]
+    for h in range(B * H):
+        ref = oracle_mod.path_product(gates[h])
+        assert np.array_equal(G[h] == 0, ref == 0) or (
+            np.all(G[h][ref == 0] == 0) and np.all(G[h][np.abs(ref) >= 2.0 ** -126] != 0))
+        big = np.abs(ref) >= 1e-30
+        assert np.max(np.abs(G[h] - ref)[big] / np.abs(ref)[big]) <= GATE_TOL
+
+
+# ------------------------------------------------------------------ chain
+
+
+def check_chain(y_gpu, y_ref, env):
+    err = np.abs(y_gpu - y_ref)
+    assert np.all(err <= GATE_TOL * env + 1e-30), float(np.max(err / np.maximum(env, 1e-300)))
+
+
+@pytest.mark.parametrize("n,dv", [(1, 16), (130, 16), (300, 64), (1000, 64), (513, 128), (777, 5)])
+def test_chain_matches_oracle(R, oracle_mod, n, dv):
+    B, H = 1, 3
+    r = np.random.default_rng(200 + n)
+    b = r.standard_normal((B * H, n, dv)).astype(np.float32)
+    u = r.uniform(0.9, 1.0, (B * H, n)).astype(np.float32)
+    u[r.uniform(size=u.shape) < 0.01] = 0.0
+    th = r.uniform(-math.pi, math.pi, (B * H, n)).astype(np.float32)
+    gs = [1.0, 0.5, 0.0]
+    yr, yi = R.chain_scan(dev(u.reshape(B, H, n)), dev(th.reshape(B, H, n)), gs,
+                          dev(b.reshape(B, H, n, dv)))
+    y = (yr.cpu().double().numpy() + 1j * yi.cpu().double().numpy()).reshape(B * H, n, dv)
+    ref, env, st = oracle_mod.chain_heads(u, th, f32(gs), b)
+    assert np.all(st == 0)
+    check_chain(y, ref, env)
+
+
+def test_chain_workload_full_size(R, oracle_mod):
+    """The path-product corner chain at full size (B=2 H=16 n=65536 dv=64), every output."""
+    ci = W.chain()
+    shp = (ci.B, ci.H, ci.n)
+    yr, yi = R.chain_scan(dev(ci.u.reshape(shp)), dev(ci.theta.reshape(shp)), ci.g,
+                          dev(ci.b.reshape(*shp, ci.dv)))
+    y = (yr.cpu().double().numpy() + 1j * yi.cpu().double().numpy()).reshape(-1, ci.n, ci.dv)
+    ref, env, st = oracle_mod.chain_heads(ci.u, ci.theta, f32(ci.switches_bh()[2]), ci.b)
+    assert np.all(st == 0)
+    check_chain(y, ref, env)
+    assert np.all(y[:, 0, :] == 0)  # b_0 = 0 gives y_0 = 0, the page's start
+
+
+def test_chain_bounded_wait_reports_timeout(R):
+    """A chunk that never publishes makes the next one's bounded wait run out: the status
+    word says so and the call returns (no hang)."""
+    B, H, n, dv = 1, 1, 1024, 16
+    u = torch.full((B, H, n), 0.97, device="cuda")
+    th = torch.zeros(B, H, n, device="cuda")
+    b = torch.ones(B, H, n, dv, device="cuda")
+    R.test_set_wait_limit_ns(20_000_000)  # 20 ms
+    R.test_set_chain_withhold(3)
+    try:
+        with pytest.raises(R.DeviceTimeout):
+            R.chain_scan(u, th, 1.0, b)
+    finally:
+        R.test_set_chain_withhold(-1)
+        R.test_set_wait_limit_ns(0)
+    yr, yi = R.chain_scan(u, th, 1.0, b)  # the context is still usable
+    assert torch.isfinite(yr).all()
+
+
+# ------------------------------------------------------------------ head
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3])
+def test_tiny_workload_all_switches(R, oracle_mod, idx):
+    """B=1 H=1 n=64 d=dv=16 fp32 at (1,1,0), (0,1,0), (0,0,1), (0.5,0.7,0.3), every row."""
+    hi = W.tiny(idx)
+    O = run_head(R, hi)
+    rows = np.arange(hi.n)
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, hi.name)
+
+
+HEAD_CASES = [
+    # B, H, n, d, dv, dtype, beta, qk, g, u_range, zero_frac
+    (1, 2, 300, 64, 64, "bf16", 1.0, 1.0, 0.5, (0.9, 1.0), 0.0),
+    (1, 2, 129, 128, 128, "bf16", 1.0, 1.0, 0.0, (0.0, 1.0), 0.0),
+    (2, 1, 384, 64, 64, "bf16", 0.0, 1.0, 0.0, (0.0, 1.0), 0.0),
+    (1, 2, 260, 128, 128, "bf16", 0.5, 0.5, 0.3, (-0.5, 1.5), 0.0),
+    (1, 1, 257, 64, 64, "bf16", 1.0, 1.0, 1.0, (0.8, 1.0), 0.02),
+    (1, 1, 200, 32, 48, "bf16", 1.0, 0.7, 0.7, (0.5, 1.0), 0.0),
+    (1, 2, 131, 64, 128, "fp32", 0.7, 1.0, 0.6, (0.7, 1.0), 0.05),
+    (1, 1, 1, 64, 64, "bf16", 1.0, 1.0, 0.5, (0.0, 1.0), 0.0),
+    (1, 3, 256, 128, 64, "bf16", 1.0, 0.0, 0.5, (0.9, 1.0), 0.0),
+]
+
+
+@pytest.mark.parametrize("case", HEAD_CASES, ids=[str(i) for i in range(len(HEAD_CASES))])
+def test_head_matches_oracle(R, oracle_mod, case):
+    B, H, n, d, dv, dt, beta, qk, g, ur, zf = case
+    hi = W.head_inputs(B, H, n, d, dv, seed=300 + n + d, dtype=dt, q_scale=1 / math.sqrt(d),
+                       u_range=ur, zero_frac=zf, beta=beta, qk=qk, g=g)
+    O = run_head(R, hi)
+    rows = np.arange(n)
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, str(case))
+    if g == 0.0:
+        assert np.all(O.imag == 0)  # g = 0 removes the gates exactly: no imaginary part
+
+
+def test_mixed_switch_grid_small(R, oracle_mod):
+    """Every point of the beta x qk x g grid (27 heads), every row, n = 300 and d = 128."""
+    hi = W.mixed(B=1, H=27, n=300)
+    O = run_head(R, hi)
+    rows = np.arange(hi.n)
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, hi.name)
+
+
+def sample_rows(n, count, seed):
+    r = np.random.default_rng(seed)
+    tail = np.arange(max(0, n - 128), n)
+    pick = r.choice(n, size=min(count, n), replace=False)
+    return np.unique(np.concatenate([[0, 1, 127, 128], tail, pick]))
+
+
+@pytest.mark.parametrize("name", ["gated_softmax", "long_softmax", "mixed"])
+def test_full_size_workloads_sampled_rows(R, oracle_mod, name):
+    """The full-size workloads in the launch configuration the benchmark times; the oracle
+    checks the last 128 rows of every head plus a seeded sample."""
+    hi = W.WORKLOADS[name]()
+    O = run_head(R, hi)
+    rows = sample_rows(hi.n, 48, 11)
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, hi.name)
+
+
+# ------------------------------------------------------------------ invariants
+
+
+def test_future_never_moves_the_past(R):
+    """Rows up to t0 are bitwise unchanged when every later input changes."""
+    hi = W.head_inputs(1, 2, 400, 64, 64, seed=5, beta=1.0, qk=1.0, g=0.5, u_range=(0.8, 1.0))
+    h2 = W.head_inputs(1, 2, 400, 64, 64, seed=6, beta=1.0, qk=1.0, g=0.5, u_range=(0.8, 1.0))
+    t0 = 250
+    for a, b in ((hi.q, h2.q), (hi.k, h2.k), (hi.v, h2.v), (hi.u, h2.u), (hi.theta, h2.theta)):
+        b[:, :t0 + 1] = a[:, :t0 + 1]
+    O1, O2 = run_head(R, hi), run_head(R, h2)
+    assert np.array_equal(O1[:, :t0 + 1], O2[:, :t0 + 1])
+
+
+def test_deterministic(R):
+    hi = W.head_inputs(2, 2, 520, 128, 128, seed=9, beta=0.5, qk=1.0, g=0.3, u_range=(0.5, 1.0))
+    assert np.array_equal(run_head(R, hi), run_head(R, hi))
+
+
+def test_all_gates_closed_leaves_the_diagonal(R, oracle_mod):
+    """Closing every gate leaves G = I: O_i = W_ii V_i with W_ii = e^{qk s_ii (1 - beta)}."""
+    hi = W.head_inputs(1, 1, 200, 64, 64, seed=12, beta=1.0, qk=1.0, g=1.0, u_range=(0.0, 0.0))
+    O = run_head(R, hi)
+    assert np.max(np.abs(O[0].real - hi.v[0])) <= 1e-6
+    assert np.all(O.imag == 0)
+
+
+@pytest.mark.parametrize("what", ["q", "k", "u", "theta"])
+def test_non_finite_inputs_are_refused(R, what):
+    for qk in (1.0, 0.0):
+        hi = W.head_inputs(1, 2, 300, 64, 64, seed=13, beta=1.0, qk=qk, g=0.5)
+        getattr(hi, what).reshape(-1)[400] = np.nan
+        with pytest.raises(R.NonFinite):
+            run_head(R, hi)
+
+
+def test_non_finite_switch_is_refused_at_once(R):
+    hi = W.head_inputs(1, 2, 64, 64, 64, seed=14, beta=float("inf"), qk=1.0, g=0.5)
+    with pytest.raises(R.NonFinite):
+        run_head(R, hi)
+
+
+def test_empty_sequence(R):
+    z = torch.zeros(1, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    zu = torch.zeros(1, 2, 0, device="cuda")
+    Ore, Oim = R.head_forward(z, z, zu, zu, z, 1.0, 1.0, 0.5)
+    assert Ore.shape == (1, 2, 0, 64) and Oim.numel() == 0
