@@ -169,6 +169,31 @@ class Clocks:
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+KERNEL_SOURCES = {"head_fwd_kernel": ["head_fwd.cu", "common.cuh", "gate_products.cuh"],
+                  "chain_scan_kernel": ["chain_scan.cu", "common.cuh"]}
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from profiles/dram_traffic.txt, if the kernel's sources are
+    unchanged since that capture (else None)."""
+    import hashlib
+    m = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "gated_causal_attention_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    digest = m.hexdigest()[:16]
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as fh:
+            for line in fh:
+                parts = line.split()
+                if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                        and parts[1] == workload and parts[2] == digest:
+                    return float(parts[3])
+    except OSError:
+        pass
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -351,13 +376,15 @@ def run_ours(args):
     if is_chain:
         achieved = work / (kern / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None, "kernel": "chain_scan_kernel",
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": measured_traffic("chain_scan_kernel", args.workload), "kernel": "chain_scan_kernel",
                 "kernel_ms": kern, "peak_kind": pk_kind,
                 "algorithmic_bytes_per_launch": work}
     else:
         achieved = work / (kern / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"], "traffic": None, "kernel": "head_fwd_kernel",
+                "frac": achieved / pk["bf16_tflops"],
+                "traffic": measured_traffic("head_fwd_kernel", args.workload), "kernel": "head_fwd_kernel",
                 "kernel_ms": kern, "peak_kind": pk_kind + " burst",
                 "algorithmic_flops_per_launch": work}
 

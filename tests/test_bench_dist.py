@@ -1,0 +1,62 @@
+"""The multi-rank path of bench.py on CPU: world size 2 over gloo.
+
+Heads are independent, so each rank runs its own full batch with no collective on the data
+path; the only exchange is the max over ranks of the measured time. These tests run that
+host logic (rendezvous on 127.0.0.1, barrier, max-reduction) without a GPU.
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import bench
+    r, w, local = bench.dist_env()
+    bench.dist_init(w, "gloo")
+    bench.dist_barrier(w)
+    t = bench.dist_max(1.0 + rank, w, "cpu")  # each rank's "time"
+    q.put((r, w, local, t))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_max_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert [g[0] for g in got] == [0, 1]
+    assert all(g[1] == 2 for g in got)
+    assert all(g[3] == 2.0 for g in got)  # the max over ranks, seen by both
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.dist_max(3.5, 1, "cpu") == 3.5
+
+
+def test_work_accounting_counts_structurally_live_entries():
+    import numpy as np
+    import bench
+    u = np.array([0.0, 0.5, 0.0, 0.7, 0.9], dtype=np.float32)
+    # g = 1: m = u; zero at k = 2 (k = 0 is never read): rows 0..4 see 1, 2, 1, 2, 3 entries
+    assert bench.live_entries(u, 1.0) == 9.0
+    assert bench.live_entries(u, 0.0) == 15.0  # g = 0: every gate is 1
