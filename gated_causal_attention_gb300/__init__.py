@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.resolvent_chain_scan.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P, _P, _SZ,
                                            _P, _P]
         L.resolvent_chain_scan.restype = _I
+        L.resolvent_chain_scan_noalloc.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P,
+                                                   _P, _P]
+        L.resolvent_chain_scan_noalloc.restype = _I
         L.resolvent_status_sync.argtypes = [_P, _P]
         L.resolvent_status_sync.restype = _I
         L.resolvent_status_string.argtypes = [_I]

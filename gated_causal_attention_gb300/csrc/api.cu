@@ -372,6 +372,29 @@ rs_status resolvent_chain_scan(const float *u, const float *theta, rs_switches s
                      y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), true);
 }
 
+rs_status resolvent_chain_scan_noalloc(const float *u, const float *theta, rs_switches sw,
+                                       const float *b, int B, int H, int n, int dv, float *y_re,
+                                       float *y_im, int32_t *status_dev, void *stream)
+{
+    g_launches = 0;
+    if (B < 0 || H < 0 || n < 0) return RS_ERR_SHAPE;
+    if ((size_t)B * H == 0 || n == 0) return RS_OK;
+    if (dv <= 0) return RS_ERR_SHAPE;
+    if (dv > 128) return RS_ERR_UNSUPPORTED;
+    rs_status st = check_switches(sw, H);
+    if (st != RS_OK) return st;
+    if (!u || !theta || !b || !y_re || !y_im || !status_dev) return RS_ERR_SHAPE;
+    for (const void *p : {(const void *)u, (const void *)theta, (const void *)b, (const void *)y_re,
+                          (const void *)y_im})
+        if (!aligned16(p)) return RS_ERR_ALIGN;
+    if (resolvent_chain_workspace_bytes(B, H, n, dv) > kChainNoAllocBytes)
+        return RS_ERR_UNSUPPORTED;  // beyond the fixed scratch
+    void *scratch = nullptr;
+    if (chain_noalloc_scratch(&scratch) != cudaSuccess) return RS_ERR_CUDA;
+    return run_chain(tables_for(sw, B, H, [](const Sw &) { return true; }), u, theta, b, 0, n, dv,
+                     y_re, y_im, scratch, status_dev, static_cast<cudaStream_t>(stream), true);
+}
+
 rs_status resolvent_status_sync(int32_t *status_dev, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

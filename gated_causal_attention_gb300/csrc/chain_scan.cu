@@ -16,6 +16,8 @@
 //   4. every warp reruns its stretch from the true carry and writes y.
 // b is read once and y written once. Every wait on another chunk is bounded in time and
 // sets RS_STATUS_TIMEOUT (carry taken as 0) when it runs out, so the kernel always ends.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace rs {
@@ -320,6 +322,32 @@ cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 }
 
 }  // namespace
+
+// Scratch of resolvent_chain_scan_noalloc: one fixed array in device memory, reserved when
+// the library is loaded on a device and held until the process exits. Host code must not
+// pass `g_chain_noalloc_scratch` itself to a kernel (on the host it names a stand-in, not a
+// device address); chain_noalloc_scratch() looks up the device address once per device.
+static __device__ __align__(256) unsigned char g_chain_noalloc_scratch[kChainNoAllocBytes];
+
+cudaError_t chain_noalloc_scratch(void **ptr)
+{
+    constexpr int kMaxDevices = 64;
+    static void *addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_chain_noalloc_scratch);  // with `dev` current
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
 
 size_t chain_scratch_bytes(int slots, int n, int dv)
 {

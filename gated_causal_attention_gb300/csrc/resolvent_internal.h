@@ -67,6 +67,10 @@ struct ChainArgs {
 constexpr int kChainChunk = 128;
 size_t chain_scratch_bytes(int slots, int n, int dv);
 cudaError_t launch_chain_scan(const ChainArgs &a, const HeadTable &tab, cudaStream_t s);
+// Fixed device-side scratch for callers that cannot allocate (8 MiB).
+constexpr size_t kChainNoAllocBytes = size_t(8) << 20;
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t chain_noalloc_scratch(void **ptr);
 
 // ---------------------------------------------------------------- head kernel (K2)
 struct HeadArgs {

@@ -134,6 +134,33 @@ rs_status resolvent_chain_scan(const float *u, const float *theta, rs_switches s
                                void *workspace, size_t workspace_bytes,
                                int32_t *status_dev, void *stream);
 
+/*
+ * resolvent_chain_scan without a workspace argument: the same chain, with its scratch in a
+ * fixed 8 MiB array of device memory inside this library. (The pages have no counterpart;
+ * this entry exists for callers, not for the method.)
+ *
+ * Who needs it: callers that cannot call cudaMalloc or hand out extra device memory, e.g.
+ * code that runs inside a framework whose own pool owns all device memory and forbids side
+ * allocations, plugin hosts that pass only input and output buffers, or latency-critical
+ * loops where an allocation (and the synchronisation it can imply) is not acceptable.
+ *
+ * Limit: the sizes must need at most 8 MiB of chain scratch, i.e.
+ * resolvent_chain_workspace_bytes(B, H, n, dv) <= 8 MiB (about 1M tokens of B*H*n per 128
+ * heads at dv = 64); larger calls return RS_ERR_UNSUPPORTED and launch nothing.
+ * The array is reserved on every GPU that loads the library and held until the process
+ * exits. The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress with that device current); make that first call before any stream
+ * capture. Nothing is allocated or freed, by this library or any library it calls. The
+ * counters that must start at zero are cleared on the stream at the start of every call;
+ * the rest keeps the last call's contents. All calls share the one array, so calls that
+ * overlap on the GPU (other streams, other threads) race: serialise them.
+ * Arguments, layout, errors and results are those of resolvent_chain_scan.
+ */
+rs_status resolvent_chain_scan_noalloc(const float *u, const float *theta, rs_switches sw,
+                                       const float *b, int B, int H, int n, int dv,
+                                       float *y_re, float *y_im,
+                                       int32_t *status_dev, void *stream);
+
 /* Synchronises `stream`, reads the status word, clears it to 0 and returns RS_OK,
  * RS_ERR_NONFINITE or RS_ERR_TIMEOUT (RS_ERR_CUDA if the runtime reports an error). */
 rs_status resolvent_status_sync(int32_t *status_dev, void *stream);
