@@ -46,7 +46,15 @@ def parse():
                    help="target CPU time of the oracle sample (cpu_baseline and --impl reference)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--B", type=int, default=None, help="override the batch (smaller profiling cases)")
+    p.add_argument("--H", type=int, default=None, help="override the heads")
+    p.add_argument("--n", type=int, default=None, help="override the sequence length")
     return p.parse_args()
+
+
+def make_inputs(args):
+    kw = {k: getattr(args, k) for k in ("B", "H", "n") if getattr(args, k) is not None}
+    return W.WORKLOADS[args.workload](**kw)
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -266,7 +274,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    inp = W.WORKLOADS[args.workload]()
+    inp = make_inputs(args)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup) * 2)
     is_chain = isinstance(inp, W.ChainInputs)
     sample = (lambda: oracle_sample_chain(inp, per_step)) if is_chain else \
@@ -308,7 +316,7 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
 
-    inp = W.WORKLOADS[args.workload]()
+    inp = make_inputs(args)
     is_chain = isinstance(inp, W.ChainInputs)
     shp = (inp.B, inp.H, inp.n)
     tdev = lambda x, s, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(

@@ -272,7 +272,10 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
     const int DP = pad64(d), DVP = pad64(dv);
     const bool f32 = dtype == RS_F32;
 
-    const auto head_tabs = tables_for(sw, B, H, [](const Sw &s) { return !is_chain_head(s); });
+    // gated heads first (their tiles are heavier), then heads with g = 0 (G = 1)
+    auto head_tabs = tables_for(sw, B, H, [](const Sw &s) { return !is_chain_head(s) && s.g != 0.f; });
+    const auto plain_tabs = tables_for(sw, B, H, [](const Sw &s) { return !is_chain_head(s) && s.g == 0.f; });
+    head_tabs.insert(head_tabs.end(), plain_tabs.begin(), plain_tabs.end());
     const auto chain_tabs = tables_for(sw, B, H, [](const Sw &s) { return is_chain_head(s); });
     const auto qk0_tabs = tables_for(sw, B, H, [](const Sw &s) { return s.qk == 0.f; });
 

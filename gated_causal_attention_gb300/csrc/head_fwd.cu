@@ -4,63 +4,145 @@
 // O_i = sum_{j<=i} W_ij V_j, evaluated in the log domain of section "Evaluation and
 // refusals": the maximum of qk s_ij over the live entries (R_ij > 0) shifts the sum Z.
 //
-// One CTA owns one 128-row query tile QB of one head; thread i owns row i (the TMEM lane
-// layout of an M = 128 accumulator). Key tiles run from KB = QB-1 down to 0, then the
-// diagonal tile:
-//   * TMA brings K, V (and Q once) into 128-byte-swizzled shared memory;
-//   * tcgen05.mma forms S = Q K^T in TMEM (bf16 in, fp32 accumulate);
-//   * each thread reads its S row, masks dead entries, keeps the running live maximum M
-//     and the shifted sum Z', and writes P = 2^{t - M} (bf16) into shared memory;
-//   * across blocks the path product factors as prefix_i * C * suffix_j (gate_products.cuh):
-//     V_j is scaled by c_j = C suffix_j into [Re | Im] halves, so one MMA with N = 2 dv
-//     accumulates sum_j P_ij c_j V_j; the row factor prefix_i multiplies the accumulator
-//     once, after the last off-diagonal tile. C only ever takes more factors, so once it
-//     is exactly 0 every farther tile is dead and the loop stops;
-//   * the diagonal tile forms G_ij explicitly (one gate per step from j = i down) and runs
-//     two MMAs, Re(P G) V and Im(P G) V;
-//   * the epilogue scales by e^{(1-beta) M} Z'^{-beta}; an exact 0 stays 0.
-// Heads with g = 0 have G = 1: no gate products, no V scaling, real accumulator only.
+// One CTA owns one 128-row query tile QB of one head. Key tiles run from KB = QB-1 down to
+// 0 (the off-diagonal tiles), then the diagonal tile KB = QB. The CTA is warp-specialised
+// and software-pipelined:
+//   warp 8      TMA producer: Q once, then K and V tiles into an NS-stage ring;
+//   warp 9      MMA issuer (one thread): S(t) = Q K(t)^T into one of two TMEM S buffers,
+//               then O += P(t-1) V'(t-1) with P read from TMEM (it overwrites S);
+//   warps 0-3   softmax, thread i = query row i: live-masked running maximum M (moved
+//               only when it grows by more than 2^8, so the accumulator is rarely
+//               rescaled), P = 2^{t - M} packed to bf16 into TMEM, the shifted sum Z', the
+//               row factor prefix_i, the diagonal tile and the epilogue;
+//   warps 4-7   value preparation (gated heads), thread j = key row j: c_j = C * suffix_j,
+//               V'_j = c_j V_j as [Re | Im] bf16 halves for one MMA with N = 2 dv, and the
+//               carry C <- C * (block total) for the next key tile.
+// Across blocks the path product factors as prefix_i * C * suffix_j (gate_products.cuh);
+// C only ever gains factors, so the key tiles beyond the first exactly-zero C are exactly
+// dead and are never loaded. Inside the diagonal tile G_ij is formed one gate at a time
+// from j = i down, and two MMAs accumulate Re(P G) V and Im(P G) V.
+// Heads with g = 0 have G = 1: no gate products, no value preparation, a real accumulator.
 //
-// Every wait on an mbarrier is bounded; one that runs out sets RS_STATUS_TIMEOUT and the
-// CTA winds down (TMEM is always freed).
+// Every wait is bounded: one that runs out raises RS_STATUS_TIMEOUT, tells the other roles
+// to stop, and the CTA winds down with its TMEM freed.
 #include "gate_products.cuh"
 
 namespace rs {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr uint32_t kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region (16 KB)
+// Warpgroup roles: 0 and 1 softmax (each query row has one thread in each: keys 0-63 and
+// 64-127 of every key tile), 2 value preparation (gated heads only), then the producer
+// warpgroup: its warp 0 loads by TMA, warp 1 issues the MMAs, warp 2 counts the key tiles.
+// After the prologue the producer (and value-prep) warpgroups hand registers to the softmax
+// warpgroups (setmaxnreg); the shares add up to exactly what the launch provides:
+//   gated:   512 threads x 128 = 2 x 128 x 192 + 128 x 88 + 128 x 40
+//   ungated: 384 threads x 168 = 2 x 128 x 232 + 128 x 40
+template <bool GATED>
+struct Roles {
+    static constexpr int threads = GATED ? 512 : 384;
+    static constexpr int prod_wg = GATED ? 3 : 2;
+    static constexpr int launch_regs = GATED ? 128 : 168;
+    static constexpr int softmax_regs = GATED ? 192 : 232;
+    static constexpr int vprep_regs = 88;
+    static constexpr int prod_regs = 40;
+    static_assert(2 * 128 * softmax_regs + (GATED ? 128 * vprep_regs : 0) + 128 * prod_regs <=
+                      threads * launch_regs,
+                  "register shares exceed the launch");
+};
+constexpr uint32_t kRegion = 128 * 128;   // one 128-row x 128-byte swizzled region (16 KB)
+constexpr float kRescaleLog2 = 8.f;       // keep a stale maximum while the excess stays below 2^8
+constexpr int kBarSoftmax = 1, kBarVprep = 2;
 
-template <int DP, int DVP>
-struct Layout {
-    static constexpr uint32_t q = 0;
-    static constexpr uint32_t k = q + (DP / 64) * kRegion;
-    static constexpr uint32_t vx = k + (DP / 64) * kRegion;         // V (or V'_re) then V'_im
-    static constexpr uint32_t p = vx + 2 * (DVP / 64) * kRegion;     // P (or Re P on the diagonal)
-    static constexpr uint32_t pim = q;                               // Im P on the diagonal: Q, K are dead by then
-    static constexpr uint32_t small = p + 2 * kRegion;
-    static constexpr uint32_t c = small;                             // float2 [128] key scales c_j
-    static constexpr uint32_t rc = c + 128 * 8;                      // float  [128] |c_j|
-    static constexpr uint32_t ga = rc + 128 * 4;                     // float2 [128] gates of the query block
-    static constexpr uint32_t gm = ga + 128 * 8;                     // float  [128] |a|
-    static constexpr uint32_t bars = gm + 128 * 4;                   // 2 mbarriers
-    static constexpr uint32_t tmem_slot = bars + 16;
-    static constexpr uint32_t bytes = tmem_slot + 16;
-    static constexpr uint32_t alloc = bytes + 1024;                  // slack for 1024-byte alignment
-    static constexpr uint32_t acc_cols = 2 * DVP;
-    static constexpr uint32_t s_col = acc_cols;
-    static constexpr uint32_t tmem_cols = (acc_cols + 128 <= 256) ? 256 : 512;
+template <int DP, int DVP, bool GATED>
+struct Cfg {
+    static constexpr uint32_t q_bytes = (DP / 64) * kRegion;
+    static constexpr uint32_t k_bytes = (DP / 64) * kRegion;
+    static constexpr uint32_t v_bytes = (DVP / 64) * kRegion;
+    // Gated: Re V' goes where K was (once S(t) is done) and Im V' replaces V, when K is at
+    // least as wide as V; otherwise Re V' replaces V and Im V' takes a region of its own.
+    static constexpr bool alias = DP >= DVP;
+    static constexpr uint32_t extra = (GATED && !alias) ? v_bytes : 0;
+    static constexpr uint32_t stage_bytes = k_bytes + v_bytes + extra;
+    static constexpr uint32_t small_bytes = 8192;
+    static constexpr uint32_t budget = 227 * 1024 - 1024 - small_bytes - q_bytes;
+    static constexpr int NS = (budget / stage_bytes) >= 4 ? 4 : (int)(budget / stage_bytes);
+    static constexpr uint32_t stages = q_bytes;                       // stage s at stages + s*stage_bytes
+    // Heads with g = 0 keep K and V in separate rings instead: a K stage frees as soon as its
+    // S is done and a V stage once its P V is done, so the K loads run further ahead.
+    static constexpr bool split = !GATED;
+    static constexpr int NSV = 2;
+    static constexpr int NSK_fit = (int)((budget - NSV * v_bytes) / k_bytes);
+    static constexpr int NSK = NSK_fit >= 4 ? 4 : NSK_fit;
+    static constexpr uint32_t vring = q_bytes + NSK * k_bytes;        // V stage s at vring + s*v_bytes
+    static constexpr uint32_t small = split ? vring + NSV * v_bytes : stages + NS * stage_bytes;
+    static constexpr uint32_t rc = small;                             // float [NS][128] |c_j|
+    static constexpr uint32_t ga = rc + NS * 128 * 4;                 // float2 [128] gates of the query block
+    static constexpr uint32_t gm = ga + 128 * 8;                      // float [128] |a|
+    static constexpr uint32_t alllive = gm + 128 * 4;                 // int [NS]
+    static constexpr uint32_t hmax = (alllive + NS * 4 + 15) & ~15u;  // float [2][2][128] half-row maxima
+    static constexpr uint32_t zpart = hmax + 4 * 128 * 4;             // float [128] second half's Z'
+    static constexpr uint32_t bars = zpart + 128 * 4;                 // mbarriers
+    // q; full, empty, vprep, rc, vfull, vempty (4 each); s_full, p_full, pv_done (2 each)
+    static constexpr int nbars = 1 + 6 * 4 + 6;
+    static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, numkv, abort
+    static constexpr uint32_t end = misc + 64;
+    static constexpr uint32_t alloc = end + 1024;
+    static constexpr uint32_t acc_cols = GATED ? 2 * DVP : DVP;
+    static constexpr uint32_t s_col0 = acc_cols;                      // S buffers: 128 columns each
+    // Re V' / Im V' offsets inside a stage, and the N-atom stride of the V' operand
+    static constexpr uint32_t vre = alias ? 0 : k_bytes;
+    static constexpr uint32_t vim = alias ? k_bytes : k_bytes + v_bytes;
+    static constexpr uint32_t lbo_cplx = alias ? (DVP == 64 ? k_bytes : kRegion) : kRegion;
+    static_assert(split ? NSK >= 2 : NS >= 2, "shared memory too small for two stages");
+    static_assert(end <= 227 * 1024 - 1024, "shared memory budget");
+    static_assert(acc_cols + 256 <= 512, "TMEM budget");
 };
 
-__device__ __forceinline__ void store_p_chunk(uint32_t base, int row, int chunk16, uint4 v)
+struct Barriers {
+    // full/empty: the K+V ring (gated heads) or the K ring (g = 0); vfull/vempty: the V ring
+    uint64_t *q, *full, *empty, *vprep, *rc, *s_full, *p_full, *pv_done, *vfull, *vempty;
+};
+
+// Bounded wait on an mbarrier phase; also gives up when another role of this CTA (abort
+// flag) or another CTA (status word) reported a timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         int32_t *status)
 {
-    // chunk16: which 8-key chunk (0..15) of the 128 keys
-    const int region = chunk16 >> 3, c = chunk16 & 7;
-    const uint32_t addr = base + region * kRegion + row * 128 + ((c ^ (row & 7)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(addr, parity)) return true;
+        if (*abort) return false;
+        if (*reinterpret_cast<volatile int32_t *>(status) & RS_STATUS_TIMEOUT_BIT) {
+            *abort = 1;
+            return false;
+        }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            flag_status(status, RS_STATUS_TIMEOUT_BIT);
+            return false;
+        }
+    }
+}
+
+// The same, with one answer for the whole warp (the warp then stays converged for the
+// warp-wide tcgen05.ld / tcgen05.st that follow).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                              int32_t *status)
+{
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status));
+}
+
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    RS_TMEM_LD32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
@@ -79,7 +161,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
                  : "memory");
 }
 
-// Multiplies this thread's accumulator row (ncols fp32 columns from `col`) by alpha.
+// acc row <- alpha * acc row (ncols fp32 columns)
 __device__ __forceinline__ void scale_acc_row(uint32_t trow, int ncols, float alpha)
 {
     for (int cc = 0; cc < ncols; cc += 32) {
@@ -93,7 +175,7 @@ __device__ __forceinline__ void scale_acc_row(uint32_t trow, int ncols, float al
     tmem_st_wait();
 }
 
-// Complex row factor: acc_re + i acc_im <- z * (acc_re + i acc_im).
+// (acc_re + i acc_im) <- z * (acc_re + i acc_im)
 __device__ __forceinline__ void cscale_acc_row(uint32_t trow, int dvp, cplx z)
 {
     for (int cc = 0; cc < dvp; cc += 32) {
@@ -113,414 +195,609 @@ __device__ __forceinline__ void cscale_acc_row(uint32_t trow, int dvp, cplx z)
     tmem_st_wait();
 }
 
-template <int DP, int DVP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int DP, int DVP, bool GATED>
+__global__ void __launch_bounds__(Roles<GATED>::threads, 1)
 head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv)
 {
-    using L = Layout<DP, DVP>;
+    using L = Cfg<DP, DVP, GATED>;
+    using RL = Roles<GATED>;
+    constexpr int NS = L::NS;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    uint64_t *bar_tma = reinterpret_cast<uint64_t *>(smem + L::bars);
-    uint64_t *bar_mma = bar_tma + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::tmem_slot);
-    float2 *s_c = reinterpret_cast<float2 *>(smem + L::c);
+    uint64_t *bar0 = reinterpret_cast<uint64_t *>(smem + L::bars);
+    Barriers B{bar0,      bar0 + 1,  bar0 + 5,  bar0 + 9,  bar0 + 13,
+               bar0 + 17, bar0 + 19, bar0 + 21, bar0 + 23, bar0 + 27};
+    int *misc = reinterpret_cast<int *>(smem + L::misc);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
+    int *s_numkv = misc + 1;
+    volatile int *s_abort = misc + 2;
     float *s_rc = reinterpret_cast<float *>(smem + L::rc);
     float2 *s_ga = reinterpret_cast<float2 *>(smem + L::ga);
     float *s_gm = reinterpret_cast<float *>(smem + L::gm);
+    int *s_alllive = reinterpret_cast<int *>(smem + L::alllive);
+    float *s_hmax = reinterpret_cast<float *>(smem + L::hmax);  // [2 tiles][2 halves][128 rows]
+    float *s_zpart = reinterpret_cast<float *>(smem + L::zpart);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
+    const int kTmaWarp = RL::prod_wg * 4, kMmaWarp = RL::prod_wg * 4 + 1;
     const int n = a.n;
     const int nqt = (n + 127) / 128;
     const int QB = nqt - 1 - (int)(blockIdx.x / tab.count);
     const int slot = (int)(blockIdx.x % tab.count);
     const int bh = tab.bh[slot];
-    const float beta = tab.beta[slot], qk = tab.qk[slot], g = tab.g[slot];
-    const bool gated = g != 0.f;
-    const bool qk_on = qk != 0.f;
+    const float beta = tab.beta[slot], qk = tab.qk[slot];
     const int sQ = QB * 128;
-    const int row = sQ + tid;
-    const bool valid = row < n;
     const int64_t tok0 = (int64_t)bh * n;
 
-    if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+    // ------------------------------------------------------------ prologue
+    if (warp == kTmaWarp && lane == 0) {
+        for (int i = 0; i < L::nbars; ++i) {
+            const uint64_t *b = bar0 + i;
+            uint32_t count = 1;                                       // TMA / tcgen05.commit
+            if (b >= B.vprep && b < B.vprep + 8) count = 128;         // value-prep threads (vprep, rc)
+            if (b >= B.p_full && b < B.p_full + 2) count = 256;       // both softmax halves
+            mbar_init(bar0 + i, count);
+        }
+        *s_abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+        // Q does not depend on anything the prologue works out: start it now
+        mbar_arrive_expect_tx(B.q, L::q_bytes);
+        for (int r = 0; r < DP / 64; ++r)
+            tma_load_3d(smem + r * kRegion, &tq, B.q, r * 64, sQ, bh);
     }
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, L::tmem_cols);
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
-    const uint32_t t_acc = tmem, t_s = tmem + L::s_col;
-
-    const float scale2 = qk * 1.4426950408889634f / sqrtf((float)a.d);  // qk log2(e) / sqrt(d)
-    const uint32_t kv_bytes = (DP / 64 + DVP / 64) * kRegion;             // K and V tiles
-    const uint32_t q_bytes = (DP / 64) * kRegion;
-    constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc_pv_real = idesc_bf16(128, DVP, false, true);
-    constexpr uint32_t idesc_pv_cplx = idesc_bf16(128, 2 * DVP, false, true);
-
-    uint32_t ph_tma = 0, ph_mma = 0;
-    bool ok = true;           // no wait has run out (uniform: every thread waits on the same barriers)
-    bool q_loaded = false;
-    bool acc_started = false;
-
-    // row state
+    // softmax threads (two per row: one per half of the key tile): the row factor prefix_i
+    const bool softmax = wg < 2;
+    const int r = tid & 127;  // query row (softmax) or key row (value prep)
+    const int row = sQ + r;
+    const bool valid = softmax && row < n;
     cplx pq = {0.f, 0.f};
     float rq = 0.f;
-    if (gated && valid) {
-        const float2 v = a.prefix[tok0 + row];
-        pq = {v.x, v.y};
-        rq = cabs(pq);
-    } else if (valid) {
-        pq = {1.f, 0.f};  // ungated: every gate is 1
-        rq = 1.f;
-    }
-    float M2 = -INFINITY;  // running live maximum of qk s log2(e)
-    float Zs = 0.f;        // sum of R 2^{t - M}
-    float chk = 0.f;       // becomes NaN if any evaluated logit is not finite
-
-    auto load_tiles = [&](int kb) {
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_tma, kv_bytes + (q_loaded ? 0u : q_bytes));
-            if (!q_loaded)
-                for (int r = 0; r < DP / 64; ++r)
-                    tma_load_3d(smem + L::q + r * kRegion, &tq, bar_tma, r * 64, sQ, bh);
-            for (int r = 0; r < DP / 64; ++r)
-                tma_load_3d(smem + L::k + r * kRegion, &tk, bar_tma, r * 64, kb * 128, bh);
-            for (int r = 0; r < DVP / 64; ++r)
-                tma_load_3d(smem + L::vx + r * kRegion, &tv, bar_tma, r * 64, kb * 128, bh);
-        }
-        q_loaded = true;
-    };
-    // Waits are bounded; `ok` turns false when one runs out. It is made uniform across the
-    // CTA (__syncthreads_and) before any decision that changes control flow.
-    auto wait_tma = [&]() {
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_tma, ph_tma, kWaitLimitNs));
-        ph_tma ^= 1;
-    };
-    auto wait_mma = [&]() {
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_mma, ph_mma, kWaitLimitNs));
-        ph_mma ^= 1;
-        tc_fence_after();
-    };
-    auto issue_s = [&]() {
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < DP / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                umma_bf16_ss(t_s, sw128_desc(sbase + L::q + off, 16, 1024),
-                             sw128_desc(sbase + L::k + off, 16, 1024), idesc_s, ks > 0);
-            }
-            umma_commit(bar_mma);
-        }
-    };
-    auto load_s_row = [&](float (&s)[128]) {
-#pragma unroll
-        for (int cc = 0; cc < 128; cc += 32) {
-            uint32_t r[32];
-            RS_TMEM_LD32(trow + L::s_col + cc, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[cc + e] = __uint_as_float(r[e]);
-        }
-    };
-
-    // -------------------------------------------------------------- off-diagonal tiles
-    const int rows_alive = __syncthreads_or(valid && (!gated || rq > 0.f));
-    cplx C = {1.f, 0.f};
-    for (int KB = QB - 1; KB >= 0 && rows_alive && ok; --KB) {
-        if (gated && !cnonzero(C)) break;  // every farther key tile is exactly dead
-        load_tiles(KB);
-        if (gated) {
-            const float2 sg = a.suffix[tok0 + KB * 128 + tid];
-            const cplx c = key_scale(C, {sg.x, sg.y});
-            s_c[tid] = make_float2(c.re, c.im);
-            s_rc[tid] = cabs(c);
-        }
-        wait_tma();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-
-        float s[128];
-        if (qk_on) {
-            issue_s();
-            wait_mma();
-            load_s_row(s);
+    if (valid) {
+        if (GATED) {
+            const float2 v = a.prefix[tok0 + row];
+            pq = {v.x, v.y};
+            rq = cabs(pq);
         } else {
-#pragma unroll
-            for (int j = 0; j < 128; ++j) s[j] = 0.f;
+            pq = {1.f, 0.f};
+            rq = 1.f;
         }
+    }
+    if (GATED && wg == 2) {  // the query block's own gates, for the diagonal tile
+        float2 av = make_float2(0.f, 0.f);
+        if (sQ + r < n) av = a.gate[tok0 + sQ + r];
+        s_ga[r] = av;
+        s_gm[r] = cabs({av.x, av.y});
+    }
+    tc_fence_before();
+    const int rows_alive = __syncthreads_or(valid && rq > 0.f);
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-        // live maximum of this tile
-        float mt = -INFINITY;
+    // number of off-diagonal key tiles: stop at the first tile whose carry C is exactly 0
+    if (warp == RL::prod_wg * 4 + 2) {
+        int numkv = rows_alive ? QB : 0;
+        if (GATED && numkv > 0) {
+            const float2 *T = a.carry + (int64_t)bh * nqt;
+            cplx run = {1.f, 0.f};
+            for (int base = 0; base < QB; base += 32) {
+                const int t = base + lane;
+                cplx x = {1.f, 0.f};
+                if (t < QB) {
+                    const float2 v = T[QB - 1 - t];
+                    x = {v.x, v.y};
+                }
+                cplx incl = x;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
-            const float4 w = gated ? *reinterpret_cast<const float4 *>(s_rc + j)
-                                   : make_float4(1.f, 1.f, 1.f, 1.f);
-            const float wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float t2 = s[j + e] * scale2;
-                s[j + e] = t2;
-                chk = fmaf(t2, 0.f, chk);
-                const bool live = valid && rq * wv[e] > 0.f;
-                mt = live ? fmaxf(mt, t2) : mt;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const cplx y = shfl_up(incl, d);
+                    if (lane >= d) incl = cmul(y, incl);
+                }
+                cplx excl = shfl_up(incl, 1);
+                if (lane == 0) excl = {1.f, 0.f};
+                const cplx Ct = cmul(run, excl);  // carry of tile t
+                const unsigned z = __ballot_sync(0xffffffffu, t < QB && !cnonzero(Ct));
+                if (z) {
+                    numkv = base + __ffs(z) - 1;
+                    break;
+                }
+                run = cmul(run, shfl_idx(incl, 31));
             }
         }
-        const float mnew = fmaxf(M2, mt);
-        float alpha = 1.f;
-        if (mnew > M2) {
-            alpha = (M2 == -INFINITY) ? 0.f : ex2_approx(M2 - mnew);
-            Zs *= alpha;
-            M2 = mnew;
-        }
-        if (__any_sync(0xffffffffu, acc_started && alpha != 1.f))
-            scale_acc_row(trow, gated ? 2 * DVP : DVP, acc_started ? alpha : 1.f);
+        if (lane == 0) *s_numkv = numkv;
+    }
+    __syncthreads();
+    const int numkv = *s_numkv;
+    const int T = numkv + 1;  // tiles: numkv off-diagonal, then the diagonal
 
-        // P = 2^{t - M} on live entries, Z' += |c_j| P
-#pragma unroll
-        for (int j = 0; j < 128; j += 8) {
-            const float4 w0 = gated ? *reinterpret_cast<const float4 *>(s_rc + j)
-                                    : make_float4(1.f, 1.f, 1.f, 1.f);
-            const float4 w1 = gated ? *reinterpret_cast<const float4 *>(s_rc + j + 4)
-                                    : make_float4(1.f, 1.f, 1.f, 1.f);
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            float p[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const bool live = valid && rq * wv[e] > 0.f;
-                p[e] = live ? ex2_approx(s[j + e] - M2) : 0.f;
-                Zs = fmaf(wv[e], p[e], Zs);
+    // Registers move from the producer (and value-prep) warps to the softmax warps: each role
+    // starts with its setmaxnreg; the shares add up to exactly what the CTA was launched with.
+    if (wg == RL::prod_wg) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RL::prod_regs));
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && L::split) {  // the K ring
+            for (int t = 0; t < T; ++t) {
+                const int st = t % L::NSK;
+                if (t >= L::NSK && !wait_bar(B.empty + st, ((t / L::NSK) - 1) & 1, s_abort, a.status)) break;
+                const int kb = t < numkv ? QB - 1 - t : QB;
+                unsigned char *stg = smem + L::stages + st * L::k_bytes;
+                mbar_arrive_expect_tx(B.full + st, L::k_bytes);
+                for (int rr = 0; rr < DP / 64; ++rr)
+                    tma_load_3d(stg + rr * kRegion, &tk, B.full + st, rr * 64, kb * 128, bh);
             }
-            store_p_chunk(sbase + L::p, tid, j >> 3,
-                          make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                                     pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+        } else if (lane == 0) {
+            for (int t = 0; t < T; ++t) {
+                const int st = t % NS;
+                if (t >= NS && !wait_bar(B.empty + st, ((t / NS) - 1) & 1, s_abort, a.status)) break;
+                const int kb = t < numkv ? QB - 1 - t : QB;
+                unsigned char *stg = smem + L::stages + st * L::stage_bytes;
+                mbar_arrive_expect_tx(B.full + st, L::k_bytes + L::v_bytes);
+                for (int rr = 0; rr < DP / 64; ++rr)
+                    tma_load_3d(stg + rr * kRegion, &tk, B.full + st, rr * 64, kb * 128, bh);
+                for (int rr = 0; rr < DVP / 64; ++rr)
+                    tma_load_3d(stg + L::k_bytes + rr * kRegion, &tv, B.full + st, rr * 64, kb * 128, bh);
+            }
         }
-
-        // V'_j = c_j V_j: Re in place, Im into the second half (thread = key row)
-        if (gated) {
-            const float2 c = s_c[tid];
+    } else if (L::split && warp == kTmaWarp + 3) {
+        // ------------------------------------------------------------ TMA producer, V ring
+        if (lane == 0) {
+            for (int t = 0; t < T; ++t) {
+                const int sv = t % L::NSV;
+                if (t >= L::NSV && !wait_bar(B.vempty + sv, ((t / L::NSV) - 1) & 1, s_abort, a.status)) break;
+                const int kb = t < numkv ? QB - 1 - t : QB;
+                unsigned char *stg = smem + L::vring + sv * L::v_bytes;
+                mbar_arrive_expect_tx(B.vfull + sv, L::v_bytes);
+                for (int rr = 0; rr < DVP / 64; ++rr)
+                    tma_load_3d(stg + rr * kRegion, &tv, B.vfull + sv, rr * 64, kb * 128, bh);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, GATED ? 2 * DVP : DVP, false, true);
+            constexpr uint32_t idesc_pv_half = idesc_bf16(128, DVP, false, true);
+            bool ok = wait_bar(B.q, 0, s_abort, a.status);
+            auto issue_pv = [&](int t) -> bool {
+                const int st = t % NS, sb = t & 1, sv = t % L::NSV;
+                if (!wait_bar(B.p_full + sb, (t >> 1) & 1, s_abort, a.status)) return false;
+                if (GATED && t < numkv && !wait_bar(B.vprep + st, (t / NS) & 1, s_abort, a.status))
+                    return false;
+                if (L::split && !wait_bar(B.vfull + sv, (t / L::NSV) & 1, s_abort, a.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t stg = sbase + L::stages + st * L::stage_bytes;
+                // the raw V tile: in its own ring (g = 0) or behind K in the shared stage
+                const uint32_t vraw = L::split ? sbase + L::vring + sv * L::v_bytes : stg + L::k_bytes;
+                // P overwrites its own S buffer, except on the diagonal, whose P is written
+                // to the other buffer while its S is still being read
+                const uint32_t pcol = tmem + L::s_col0 + (t < numkv ? sb : (sb ^ 1)) * 128;
+                if (t < numkv) {
+                    const uint32_t vbase = GATED ? stg + L::vre : vraw;
+                    const uint32_t lbo = GATED ? L::lbo_cplx : kRegion;
 #pragma unroll
-            for (int r = 0; r < DVP / 64; ++r) {
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_bf16_ts(tmem, pcol + ks * 8, sw128_desc(vbase + ks * 2048, lbo, 1024),
+                                     idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+                } else {  // diagonal tile: raw V, Re(P G) and Im(P G) from the two halves of S
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t bd = sw128_desc(vraw + ks * 2048, kRegion, 1024);
+                        umma_bf16_ts(tmem, pcol + ks * 8, bd, idesc_pv_half, (t > 0 || ks > 0) ? 1u : 0u);
+                        if (GATED)
+                            umma_bf16_ts(tmem + DVP, pcol + 64 + ks * 8, bd, idesc_pv_half,
+                                         (t > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                umma_commit(B.pv_done + sb);
+                umma_commit(L::split ? B.vempty + sv : B.empty + st);
+                return true;
+            };
+            for (int t = 0; ok && t < T; ++t) {
+                const int nsk = L::split ? L::NSK : NS;  // stages of the ring that holds K
+                const int st = t % nsk, sb = t & 1;
+                if (!wait_bar(B.full + st, (t / nsk) & 1, s_abort, a.status)) { ok = false; break; }
+                if (t >= 2 && !wait_bar(B.pv_done + sb, ((t - 2) >> 1) & 1, s_abort, a.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t kst = sbase + L::stages + st * (L::split ? L::k_bytes : L::stage_bytes);
+#pragma unroll
+                for (int ks = 0; ks < DP / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
+                    umma_bf16_ss(tmem + L::s_col0 + sb * 128, sw128_desc(sbase + off, 16, 1024),
+                                 sw128_desc(kst + off, 16, 1024), idesc_s, ks > 0);
+                }
+                umma_commit(B.s_full + sb);
+                if (L::split) umma_commit(B.empty + st);  // the K stage is free once S is done
+                if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+            }
+            if (ok) issue_pv(T - 1);
+        }
+    }
+    } else if (GATED && wg == 2) {
+        // ------------------------------------------------------------ value preparation
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RL::vprep_regs));
+        const int j = r;
+        cplx C = {1.f, 0.f};
+        const float2 *Tc = a.carry + (int64_t)bh * nqt;
+        for (int t = 0; t < numkv; ++t) {
+            const int st = t % NS;
+            const int kb = QB - 1 - t;
+            const float2 sgv = a.suffix[tok0 + kb * 128 + j];
+            const float2 Tv = Tc[kb];
+            // a wait that runs out sets the abort flag; the group leaves together after the
+            // barrier below, so no thread is left waiting on it. (The stage being full also
+            // means the softmax rows are done with this stage's previous |c_j|.)
+            wait_bar(B.full + st, (t / NS) & 1, s_abort, a.status);
+            const cplx c = key_scale(C, {sgv.x, sgv.y});
+            const float rc = cabs(c);
+            s_rc[st * 128 + j] = rc;
+            const bool all = named_bar_and(kBarVprep, 128, rc > 0.f);
+            if (*s_abort) break;
+            s_alllive[st] = all;
+            mbar_arrive(B.rc + st);  // the softmax rows need only |c_j|
+            if (L::alias) wait_bar(B.s_full + (t & 1), (t >> 1) & 1, s_abort, a.status);
+            // V'_j = c_j V_j: Re and Im halves, same swizzled position as V_j
+            const uint32_t stg = sbase + L::stages + st * L::stage_bytes;
+#pragma unroll
+            for (int rr = 0; rr < DVP / 64; ++rr) {
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t addr = sbase + L::vx + r * kRegion + tid * 128 + ch * 16;
-                    const uint4 v = lds128(addr);
+                    // rows are 128 B apart: rotate the chunk order by the row so that a
+                    // warp's 16-byte accesses spread over all banks
+                    const uint32_t off = rr * kRegion + j * 128 + ((ch + j) & 7) * 16;
+                    const uint4 v = lds128(stg + L::k_bytes + off);
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                     uint32_t ore[4], oim[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = unpack_bf16x2(w[e]);
-                        ore[e] = pack_bf16x2(f.x * c.x, f.y * c.x);
-                        oim[e] = pack_bf16x2(f.x * c.y, f.y * c.y);
+                        ore[e] = pack_bf16x2(f.x * c.re, f.y * c.re);
+                        oim[e] = pack_bf16x2(f.x * c.im, f.y * c.im);
                     }
-                    sts128(addr, make_uint4(ore[0], ore[1], ore[2], ore[3]));
-                    sts128(addr + (DVP / 64) * kRegion, make_uint4(oim[0], oim[1], oim[2], oim[3]));
+                    sts128(stg + L::vre + off, make_uint4(ore[0], ore[1], ore[2], ore[3]));
+                    sts128(stg + L::vim + off, make_uint4(oim[0], oim[1], oim[2], oim[3]));
                 }
             }
+            fence_proxy_async_smem();
+            mbar_arrive(B.vprep + st);
+            C = carry_step(C, {Tv.x, Tv.y});
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        if (tid == 0) {
+    } else if (softmax) {
+        // ------------------------------------------------------------ softmax rows
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RL::softmax_regs));
+        // Two threads per query row: half h takes keys [64h, 64h + 64) of every key tile.
+        const int h = wg;
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float scale2 = qk * 1.4426950408889634f / sqrtf((float)a.d);  // qk log2(e)/sqrt(d)
+        const bool qk_on = qk != 0.f;
+        float M2 = -INFINITY;  // (stale) running live maximum, log2 units (same in both halves)
+        float Zs = 0.f;        // this half's sum of R 2^{t - M}
+        float chk = 0.f;       // turns NaN if an evaluated logit is not finite
+        bool ok = true;
+
+        for (int t = 0; t < numkv; ++t) {
+            const int st = t % NS, sb = t & 1;
+            const uint32_t scol = trow + L::s_col0 + sb * 128;
+            bool ready = wait_bar_warp(B.s_full + sb, (t >> 1) & 1, s_abort, a.status);
+            if (GATED && ready) ready = wait_bar_warp(B.rc + st, (t / NS) & 1, s_abort, a.status);
             tc_fence_after();
-            const uint32_t idesc = gated ? idesc_pv_cplx : idesc_pv_real;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t aoff = (ks >> 2) * kRegion + (ks & 3) * 32;
-                umma_bf16_ss(t_acc, sw128_desc(sbase + L::p + aoff, 16, 1024),
-                             sw128_desc(sbase + L::vx + ks * 2048, kRegion, 1024), idesc,
-                             (acc_started || ks > 0) ? 1u : 0u);
+            const float *rcs = s_rc + st * 128 + 64 * h;
+            // fast: every entry of every valid row of this warp is live (no masking needed)
+            const bool fast = __all_sync(0xffffffffu, !GATED || !ready || (s_alllive[st] && (rq > 0.f || !valid)));
+            // this half's 64 logits stay in registers for both passes
+            uint32_t s[64];
+            if (qk_on && ready) {
+                RS_TMEM_LD32(scol + 64 * h, s);
+                RS_TMEM_LD32(scol + 64 * h + 32, (s + 32));
+                tmem_ld_wait();
             }
-            umma_commit(bar_mma);
-        }
-        wait_mma();
-        acc_started = true;
-        if (gated) {
-            const float2 T = a.carry[(int64_t)bh * nqt + KB];
-            C = carry_step(C, {T.x, T.y});
-        }
-    }
-
-    ok = __syncthreads_and(ok);
-
-    // -------------------------------------------------------------- row factor prefix_i
-    if (ok && gated && acc_started) {
-        cscale_acc_row(trow, DVP, pq);
-        Zs *= rq;
-    }
-
-    // -------------------------------------------------------------- diagonal tile
-    if (ok) {
-        load_tiles(QB);
-        if (gated) {
-            float2 av = make_float2(0.f, 0.f);
-            if (valid) av = a.gate[tok0 + row];
-            s_ga[tid] = av;
-            s_gm[tid] = cabs({av.x, av.y});
-        }
-        wait_tma();
-    }
-    ok = __syncthreads_and(ok);
-    if (ok) {
-        float s[128];
-        if (qk_on) {
-            issue_s();
-            wait_mma();
-            load_s_row(s);
-        } else {
+            // pass 1: the half-row live maximum of t = qk s log2(e)
+            float mt = -INFINITY;
+            if (qk_on && fast) {
+                // max (or min, for qk < 0) of the raw logits, then one scaling;
+                // eight independent running extrema keep the dependency chains short
+                float hx[8];
 #pragma unroll
-            for (int j = 0; j < 128; ++j) s[j] = 0.f;
-        }
-        const int i = tid;
-        // pass 1: causal logits, the live maximum
-        float mt = -INFINITY;
-        {
-            cplx G = {1.f, 0.f};
-            float R = 1.f;
+                for (int e = 0; e < 8; ++e) hx[e] = -INFINITY;
+                if (scale2 >= 0.f) {
 #pragma unroll
-            for (int j = 127; j >= 0; --j) {
-                if (gated && j < i) {
-                    const float2 an = s_ga[j + 1];
-                    G = diag_step(G, {an.x, an.y});
-                    R *= s_gm[j + 1];
+                    for (int e = 0; e < 64; ++e) hx[e & 7] = fmaxf(hx[e & 7], __uint_as_float(s[e]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) hx[e & 7] = fmaxf(hx[e & 7], -__uint_as_float(s[e]));
                 }
-                const float t2 = s[j] * scale2;
-                s[j] = t2;
-                const bool causal = valid && j <= i;
-                if (causal) chk = fmaf(t2, 0.f, chk);
-                const bool live = causal && R > 0.f;
-                mt = live ? fmaxf(mt, t2) : mt;
+                const float hm = fmaxf(fmaxf(fmaxf(hx[0], hx[1]), fmaxf(hx[2], hx[3])),
+                                       fmaxf(fmaxf(hx[4], hx[5]), fmaxf(hx[6], hx[7])));
+                mt = hm * fabsf(scale2);
+            } else if (qk_on) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const float t2 = __uint_as_float(s[e]) * scale2;
+                    mt = (rq * rcs[e] > 0.f) ? fmaxf(mt, t2) : mt;
+                }
+            } else {
+                bool any = fast;
+                if (!fast)
+                    for (int e = 0; e < 64 && !any; ++e) any = rq * rcs[e] > 0.f;
+                mt = any ? 0.f : -INFINITY;
             }
-        }
-        const float mnew = fmaxf(M2, mt);
-        float alpha = 1.f;
-        if (mnew > M2) {
-            alpha = (M2 == -INFINITY) ? 0.f : ex2_approx(M2 - mnew);
-            Zs *= alpha;
-            M2 = mnew;
-        }
-        if (__any_sync(0xffffffffu, acc_started && alpha != 1.f))
-            scale_acc_row(trow, gated ? 2 * DVP : DVP, acc_started ? alpha : 1.f);
-
-        // pass 2: P G (Re into the P buffer, Im into the dead Q/K buffer)
-        {
-            cplx G = {1.f, 0.f};
-            float R = 1.f;
-            float pre[8], pim[8];
-#pragma unroll
-            for (int j = 127; j >= 0; --j) {
-                if (gated && j < i) {
-                    const float2 an = s_ga[j + 1];
-                    G = diag_step(G, {an.x, an.y});
-                    R *= s_gm[j + 1];
-                }
-                const bool live = valid && j <= i && R > 0.f;
-                const float p = live ? ex2_approx(s[j] - M2) : 0.f;
-                Zs = fmaf(R, p, Zs);
-                pre[j & 7] = gated ? G.re * p : p;
-                pim[j & 7] = G.im * p;
-                if ((j & 7) == 0) {
-                    store_p_chunk(sbase + L::p, tid, j >> 3,
-                                  make_uint4(pack_bf16x2(pre[0], pre[1]), pack_bf16x2(pre[2], pre[3]),
-                                             pack_bf16x2(pre[4], pre[5]), pack_bf16x2(pre[6], pre[7])));
-                    if (gated)
-                        store_p_chunk(sbase + L::pim, tid, j >> 3,
-                                      make_uint4(pack_bf16x2(pim[0], pim[1]), pack_bf16x2(pim[2], pim[3]),
-                                                 pack_bf16x2(pim[4], pim[5]), pack_bf16x2(pim[6], pim[7])));
+            if (!valid) mt = -INFINITY;
+            // the two halves exchange their maxima; the barrier also makes every S read of
+            // this tile happen before either half writes P over it, and lets both halves
+            // leave together if a wait ran out
+            s_hmax[(sb * 2 + h) * 128 + r] = mt;
+            ok = named_bar_and(kBarSoftmax, 256, ready && !*s_abort);
+            if (!ok) break;
+            mt = fmaxf(mt, s_hmax[(sb * 2 + (h ^ 1)) * 128 + r]);
+            // move the maximum only when it grows by more than 2^8 (or is first set)
+            float alpha = 1.f;
+            if (mt > M2 + kRescaleLog2 || (M2 == -INFINITY && mt > -INFINITY)) {
+                alpha = (M2 == -INFINITY) ? 0.f : ex2_approx(M2 - mt);
+                M2 = mt;
+                Zs *= alpha;
+            }
+            if (h == 0 && __any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
+                // the accumulator holds P(<= t-1) V: wait for PV(t-1), then rescale
+                if (wait_bar_warp(B.pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, s_abort, a.status)) {
+                    tc_fence_after();
+                    scale_acc_row(trow, L::acc_cols, t > 0 ? alpha : 1.f);
                 }
             }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        if (ok && tid == 0) {
-            tc_fence_after();
+            // pass 2: P = 2^{t - M} on live entries (bf16, two per TMEM column), Z' += |c_j| P.
+            // A row with no live entry yet keeps M = -inf; its logits are still checked.
+            const float nMx = (M2 == -INFINITY) ? 0.f : -M2;
+            float zp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums
+            uint32_t pk[32];
+            if (fast) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t aoff = (ks >> 2) * kRegion + (ks & 3) * 32;
-                const uint64_t bdesc = sw128_desc(sbase + L::vx + ks * 2048, kRegion, 1024);
-                umma_bf16_ss(t_acc, sw128_desc(sbase + L::p + aoff, 16, 1024), bdesc, idesc_pv_real,
-                             (acc_started || ks > 0) ? 1u : 0u);
-                if (gated)
-                    umma_bf16_ss(t_acc + DVP, sw128_desc(sbase + L::pim + aoff, 16, 1024), bdesc,
-                                 idesc_pv_real, (acc_started || ks > 0) ? 1u : 0u);
+                for (int e = 0; e < 64; e += 4) {
+                    const float4 w4 = GATED ? *reinterpret_cast<const float4 *>(rcs + e)
+                                            : make_float4(1.f, 1.f, 1.f, 1.f);
+                    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    float p[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float x = qk_on ? fmaf(__uint_as_float(s[e + k]), scale2, nMx) : nMx;
+                        cp[k] = fmaf(x, 0.f, cp[k]);
+                        p[k] = valid ? ex2_approx(x) : 0.f;
+                        zp[k] = GATED ? fmaf(wv[k], p[k], zp[k]) : zp[k] + p[k];
+                    }
+                    pk[e >> 1] = pack_bf16x2(p[0], p[1]);
+                    pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    float p2[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float w = GATED ? rcs[e + k] : 1.f;
+                        const float x = qk_on ? fmaf(__uint_as_float(s[e + k]), scale2, nMx) : nMx;
+                        cp[k] = fmaf(x, 0.f, cp[k]);
+                        const bool live = valid && rq * w > 0.f;
+                        p2[k] = live ? ex2_approx(x) : 0.f;
+                        zp[k] = fmaf(w, p2[k], zp[k]);
+                    }
+                    pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                }
             }
-            umma_commit(bar_mma);
+            RS_TMEM_ST16(scol + 32 * h, pk);
+            RS_TMEM_ST16(scol + 32 * h + 16, (pk + 16));
+            Zs += (zp[0] + zp[1]) + (zp[2] + zp[3]);
+            chk += (cp[0] + cp[1]) + (cp[2] + cp[3]);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(B.p_full + sb);
         }
-        if (ok) wait_mma();
-        acc_started = true;
-    }
-    ok = __syncthreads_and(ok);
 
-    // -------------------------------------------------------------- epilogue
-    if (ok) {
-        bool bad = false;
-        float f = 0.f;
-        if (valid) {
-            bad = isnan(chk) || !isfinite(M2) || !(Zs > 0.f) || !isfinite(Zs);
-            // O = acc e^{(1-beta) M} Z'^{-beta}, in base 2; beta log Z' is 0 at beta = 0
-            f = (beta == 0.f) ? exp2f(M2) : exp2f((1.f - beta) * M2 - beta * log2f(Zs));
-        }
-        if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
-        float *ore = a.O_re + (tok0 + row) * (int64_t)a.dv;
-        float *oim = a.O_im + (tok0 + row) * (int64_t)a.dv;
-        for (int cc = 0; cc < DVP; cc += 32) {
-            uint32_t re[32], im[32];
-            RS_TMEM_LD32(trow + cc, re);
-            if (gated) RS_TMEM_LD32(trow + DVP + cc, im);
-            tmem_ld_wait();
-            if (valid) {
+        // the second half hands its partial sum to the first, which does the rest
+        if (h == 1) s_zpart[r] = Zs + chk;  // chk is 0, or NaN to refuse
+        ok = named_bar_and(kBarSoftmax, 256, ok && !*s_abort);
+        if (h == 0) {
+            Zs += s_zpart[r];
+
+            // the row factor prefix_i, once every off-diagonal product is in the accumulator
+            if (ok && GATED && numkv > 0) {
+                if (!wait_bar_warp(B.pv_done + ((numkv - 1) & 1), ((numkv - 1) >> 1) & 1, s_abort, a.status))
+                    ok = false;
+                if (ok) {
+                    tc_fence_after();
+                    cscale_acc_row(trow, DVP, pq);
+                    Zs *= rq;
+                }
+            }
+
+            // diagonal tile: G_ij formed one gate at a time from j = i down
+            const int t = numkv, sb = t & 1;
+            const uint32_t scol = trow + L::s_col0 + sb * 128;
+            if (ok && !wait_bar_warp(B.s_full + sb, (t >> 1) & 1, s_abort, a.status)) ok = false;
+            if (ok) {
+                tc_fence_after();
+                const int i = r;
+                float mt = -INFINITY;
+                {
+                    float R = 1.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int col = cc + e;
-                    if (col < a.dv) {
-                        const float xr = __uint_as_float(re[e]);
-                        const float xi = gated ? __uint_as_float(im[e]) : 0.f;
-                        ore[col] = (xr == 0.f) ? 0.f : xr * f;  // an exact 0 stays 0 (never 0 * inf)
-                        oim[col] = (xi == 0.f) ? 0.f : xi * f;
+                    for (int c = 3; c >= 0; --c) {
+                        float sv[32];
+                        if (qk_on) tmem_ld32f(scol + c * 32, sv);
+                        if (c <= warp) {
+#pragma unroll
+                            for (int e = 31; e >= 0; --e) {
+                                const int j = c * 32 + e;
+                                if (GATED && j < i) R *= s_gm[j + 1];
+                                const float t2 = qk_on ? sv[e] * scale2 : 0.f;
+                                const bool live = valid && j <= i && R > 0.f;
+                                mt = live ? fmaxf(mt, t2) : mt;
+                            }
+                        }
+                    }
+                }
+                float alpha = 1.f;
+                if (mt > M2 + kRescaleLog2 || (M2 == -INFINITY && mt > -INFINITY)) {
+                    alpha = (M2 == -INFINITY) ? 0.f : ex2_approx(M2 - mt);
+                    M2 = mt;
+                    Zs *= alpha;
+                }
+                // P of the diagonal goes to the other S buffer, free once PV(t-1) is done
+                // (gated heads waited for it above, before the row factor)
+                if (!GATED && numkv > 0 &&
+                    !wait_bar_warp(B.pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, s_abort, a.status))
+                    ok = false;
+                if (ok && __any_sync(0xffffffffu, numkv > 0 && alpha != 1.f)) {
+                    tc_fence_after();
+                    scale_acc_row(trow, L::acc_cols, numkv > 0 ? alpha : 1.f);
+                }
+            }
+            const uint32_t pdiag = trow + L::s_col0 + (sb ^ 1) * 128;
+            if (ok) {
+                const int i = r;
+                cplx G = {1.f, 0.f};
+                float R = 1.f;
+#pragma unroll
+                for (int c = 3; c >= 0; --c) {
+                    float sv[32];
+                    if (qk_on) tmem_ld32f(scol + c * 32, sv);
+                    uint32_t pre[16], pim[16];
+                    float odd_re = 0.f, odd_im = 0.f;  // key j+1 of the pair (j, j+1)
+#pragma unroll
+                    for (int e = 31; e >= 0; --e) {
+                        const int j = c * 32 + e;
+                        float pr = 0.f, pi = 0.f;
+                        if (c <= warp) {
+                            if (GATED && j < i) {
+                                const float2 an = s_ga[j + 1];
+                                G = diag_step(G, {an.x, an.y});
+                                R *= s_gm[j + 1];
+                            }
+                            const bool causal = valid && j <= i;
+                            const float x = qk_on ? fmaf(sv[e], scale2, -M2) : -M2;
+                            if (causal) chk = fmaf(x, 0.f, chk);
+                            const bool live = causal && R > 0.f;
+                            const float p = live ? ex2_approx(x) : 0.f;
+                            Zs = fmaf(R, p, Zs);
+                            pr = GATED ? G.re * p : p;
+                            pi = GATED ? G.im * p : 0.f;
+                        }
+                        // pack (j, j+1): the pair completes at even j
+                        if (e & 1) {
+                            odd_re = pr;
+                            odd_im = pi;
+                        } else {
+                            pre[e >> 1] = pack_bf16x2(pr, odd_re);
+                            pim[e >> 1] = pack_bf16x2(pi, odd_im);
+                        }
+                    }
+                    RS_TMEM_ST16(pdiag + c * 16, pre);
+                    if (GATED) RS_TMEM_ST16(pdiag + 64 + c * 16, pim);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+            }
+            // both halves arrive on p_full: the second half does so on behalf of no work
+            // (the count stays 256)
+            mbar_arrive(B.p_full + sb);
+            mbar_arrive(B.p_full + sb);
+
+            // epilogue: O = acc e^{(1-beta) M} Z'^{-beta}
+            if (ok && !wait_bar_warp(B.pv_done + sb, (t >> 1) & 1, s_abort, a.status)) ok = false;
+            if (ok) {
+                tc_fence_after();
+                bool bad = false;
+                float f = 0.f;
+                if (valid) {
+                    bad = isnan(chk) || !isfinite(M2) || !(Zs > 0.f) || !isfinite(Zs);
+                    f = (beta == 0.f) ? exp2f(M2) : exp2f((1.f - beta) * M2 - beta * log2f(Zs));
+                }
+                if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
+                float *ore = a.O_re + (tok0 + row) * (int64_t)a.dv;
+                float *oim = a.O_im + (tok0 + row) * (int64_t)a.dv;
+                const bool vec = (a.dv & 3) == 0;
+                for (int cc = 0; cc < DVP; cc += 32) {
+                    uint32_t re[32], im[32];
+                    RS_TMEM_LD32(trow + cc, re);
+                    if (GATED) RS_TMEM_LD32(trow + DVP + cc, im);
+                    tmem_ld_wait();
+                    if (valid) {
+                        if (vec && cc + 32 <= a.dv) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                float4 vr, vi;
+                                float *pr = &vr.x, *pi = &vi.x;
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const float xr = __uint_as_float(re[e + k]);
+                                    const float xi = GATED ? __uint_as_float(im[e + k]) : 0.f;
+                                    pr[k] = (xr == 0.f) ? 0.f : xr * f;  // an exact 0 stays 0 (never 0 * inf)
+                                    pi[k] = (xi == 0.f) ? 0.f : xi * f;
+                                }
+                                *reinterpret_cast<float4 *>(ore + cc + e) = vr;
+                                *reinterpret_cast<float4 *>(oim + cc + e) = vi;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (cc + e < a.dv) {
+                                    const float xr = __uint_as_float(re[e]);
+                                    const float xi = GATED ? __uint_as_float(im[e]) : 0.f;
+                                    ore[cc + e] = (xr == 0.f) ? 0.f : xr * f;
+                                    oim[cc + e] = (xi == 0.f) ? 0.f : xi * f;
+                                }
+                        }
                     }
                 }
             }
         }
-    } else if (tid == 0) {
-        flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
     }
 
+    // ------------------------------------------------------------ teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, L::tmem_cols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
-template <int DP, int DVP>
+template <int DP, int DVP, bool GATED>
 cudaError_t launch_t(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
                      const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s)
 {
-    using L = Layout<DP, DVP>;
-    auto k = head_fwd_kernel<DP, DVP>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
+    using L = Cfg<DP, DVP, GATED>;
+    auto k = head_fwd_kernel<DP, DVP, GATED>;
+    // The register hand-over inside the kernel assumes the launch register count; a build
+    // that came out smaller would make setmaxnreg.inc wait forever, so refuse to launch it.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, k);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs < Roles<GATED>::launch_regs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
     if (e != cudaSuccess) return e;
     const int nqt = (a.n + 127) / 128;
-    k<<<nqt * tab.count, kThreads, L::alloc, s>>>(a, tab, tq, tk, tv);
+    k<<<nqt * tab.count, Roles<GATED>::threads, L::alloc, s>>>(a, tab, tq, tk, tv);
     return cudaGetLastError();
+}
+
+template <bool GATED>
+cudaError_t launch_g(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
+                     const CUtensorMap &tk, const CUtensorMap &tv, int dpad, int dvpad,
+                     cudaStream_t s)
+{
+    if (dpad == 64 && dvpad == 64) return launch_t<64, 64, GATED>(a, tab, tq, tk, tv, s);
+    if (dpad == 64 && dvpad == 128) return launch_t<64, 128, GATED>(a, tab, tq, tk, tv, s);
+    if (dpad == 128 && dvpad == 64) return launch_t<128, 64, GATED>(a, tab, tq, tk, tv, s);
+    return launch_t<128, 128, GATED>(a, tab, tq, tk, tv, s);
 }
 
 }  // namespace
@@ -530,10 +807,9 @@ cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const CUten
                             cudaStream_t s)
 {
     if (tab.count == 0 || a.n == 0) return cudaSuccess;
-    if (dpad == 64 && dvpad == 64) return launch_t<64, 64>(a, tab, tq, tk, tv, s);
-    if (dpad == 64 && dvpad == 128) return launch_t<64, 128>(a, tab, tq, tk, tv, s);
-    if (dpad == 128 && dvpad == 64) return launch_t<128, 64>(a, tab, tq, tk, tv, s);
-    return launch_t<128, 128>(a, tab, tq, tk, tv, s);
+    // one launch serves heads of one kind: the caller splits gated and ungated heads
+    return tab.g[0] != 0.f ? launch_g<true>(a, tab, tq, tk, tv, dpad, dvpad, s)
+                           : launch_g<false>(a, tab, tq, tk, tv, dpad, dvpad, s);
 }
 
 }  // namespace rs
