@@ -36,16 +36,16 @@ namespace {
 // warpgroup: its warp 0 loads by TMA, warp 1 issues the MMAs, warp 2 counts the key tiles.
 // After the prologue the producer (and value-prep) warpgroups hand registers to the softmax
 // warpgroups (setmaxnreg); the shares add up to exactly what the launch provides:
-//   gated:   512 threads x 128 = 2 x 128 x 192 + 128 x 88 + 128 x 40
-//   ungated: 384 threads x 168 = 2 x 128 x 232 + 128 x 40
+//   gated:   512 threads x 128 = 2 x 128 x 184 + 128 x 80 + 128 x 64
+//   ungated: 384 threads x 168 >= 2 x 128 x 216 + 128 x 64
 template <bool GATED>
 struct Roles {
     static constexpr int threads = GATED ? 512 : 384;
     static constexpr int prod_wg = GATED ? 3 : 2;
     static constexpr int launch_regs = GATED ? 128 : 168;
-    static constexpr int softmax_regs = GATED ? 192 : 232;
-    static constexpr int vprep_regs = 88;
-    static constexpr int prod_regs = 40;
+    static constexpr int softmax_regs = GATED ? 184 : 216;
+    static constexpr int vprep_regs = 80;
+    static constexpr int prod_regs = 64;
     static_assert(2 * 128 * softmax_regs + (GATED ? 128 * vprep_regs : 0) + 128 * prod_regs <=
                       threads * launch_regs,
                   "register shares exceed the launch");
@@ -83,20 +83,22 @@ struct Cfg {
     static constexpr uint32_t hmax = (alllive + NS * 4 + 15) & ~15u;  // float [2][2][128] half-row maxima
     static constexpr uint32_t zpart = hmax + 4 * 128 * 4;             // float [128] second half's Z'
     static constexpr uint32_t bars = zpart + 128 * 4;                 // mbarriers
-    // q; full, empty, vprep, rc, vfull, vempty (4 each); s_full, p_full, pv_done (2 each)
-    static constexpr int nbars = 1 + 6 * 4 + 6;
+    // q; full, empty, vprep, rc (4 each); s_full, p_full, pv_done (3 each); vfull, vempty (4 each)
+    static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4;
     static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, numkv, abort
     static constexpr uint32_t end = misc + 64;
     static constexpr uint32_t alloc = end + 1024;
     static constexpr uint32_t acc_cols = GATED ? 2 * DVP : DVP;
     static constexpr uint32_t s_col0 = acc_cols;                      // S buffers: 128 columns each
+    // Three S buffers where TMEM allows: S(t) then never waits for P(t-2) V to finish
+    static constexpr int NSB = acc_cols <= 128 ? 3 : 2;
     // Re V' / Im V' offsets inside a stage, and the N-atom stride of the V' operand
     static constexpr uint32_t vre = alias ? 0 : k_bytes;
     static constexpr uint32_t vim = alias ? k_bytes : k_bytes + v_bytes;
     static constexpr uint32_t lbo_cplx = alias ? (DVP == 64 ? k_bytes : kRegion) : kRegion;
     static_assert(split ? NSK >= 2 : NS >= 2, "shared memory too small for two stages");
     static_assert(end <= 227 * 1024 - 1024, "shared memory budget");
-    static_assert(acc_cols + 256 <= 512, "TMEM budget");
+    static_assert(acc_cols + NSB * 128 <= 512, "TMEM budget");
 };
 
 struct Barriers {
@@ -106,15 +108,19 @@ struct Barriers {
 
 // Bounded wait on an mbarrier phase; also gives up when another role of this CTA (abort
 // flag) or another CTA (status word) reported a timeout.
+// Roles off the critical path pass sleep_ns > 0 and nap between polls, so that their
+// spinning does not take issue slots from the softmax warps sharing their SM sub-partition.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                         int32_t *status)
+                                         int32_t *status, uint32_t sleep_ns = 0)
 {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 32; ++i) {
             if (mbar_try_wait(addr, parity)) return true;
+            if (sleep_ns) __nanosleep(sleep_ns);
+        }
         if (*abort) return false;
         if (*reinterpret_cast<volatile int32_t *>(status) & RS_STATUS_TIMEOUT_BIT) {
             *abort = 1;
@@ -133,7 +139,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
                                               int32_t *status)
 {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status));
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status, 32));
 }
 
 __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32])
@@ -210,7 +216,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bar0 = reinterpret_cast<uint64_t *>(smem + L::bars);
     Barriers B{bar0,      bar0 + 1,  bar0 + 5,  bar0 + 9,  bar0 + 13,
-               bar0 + 17, bar0 + 19, bar0 + 21, bar0 + 23, bar0 + 27};
+               bar0 + 17, bar0 + 20, bar0 + 23, bar0 + 26, bar0 + 30};
     int *misc = reinterpret_cast<int *>(smem + L::misc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     int *s_numkv = misc + 1;
@@ -239,7 +245,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             const uint64_t *b = bar0 + i;
             uint32_t count = 1;                                       // TMA / tcgen05.commit
             if (b >= B.vprep && b < B.vprep + 8) count = 128;         // value-prep threads (vprep, rc)
-            if (b >= B.p_full && b < B.p_full + 2) count = 256;       // both softmax halves
+            if (b >= B.p_full && b < B.p_full + 3) count = 256;       // both softmax halves
             mbar_init(bar0 + i, count);
         }
         *s_abort = 0;
@@ -329,7 +335,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         if (lane == 0 && L::split) {  // the K ring
             for (int t = 0; t < T; ++t) {
                 const int st = t % L::NSK;
-                if (t >= L::NSK && !wait_bar(B.empty + st, ((t / L::NSK) - 1) & 1, s_abort, a.status)) break;
+                if (t >= L::NSK && !wait_bar(B.empty + st, ((t / L::NSK) - 1) & 1, s_abort, a.status, 256)) break;
                 const int kb = t < numkv ? QB - 1 - t : QB;
                 unsigned char *stg = smem + L::stages + st * L::k_bytes;
                 mbar_arrive_expect_tx(B.full + st, L::k_bytes);
@@ -339,7 +345,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         } else if (lane == 0) {
             for (int t = 0; t < T; ++t) {
                 const int st = t % NS;
-                if (t >= NS && !wait_bar(B.empty + st, ((t / NS) - 1) & 1, s_abort, a.status)) break;
+                if (t >= NS && !wait_bar(B.empty + st, ((t / NS) - 1) & 1, s_abort, a.status, 256)) break;
                 const int kb = t < numkv ? QB - 1 - t : QB;
                 unsigned char *stg = smem + L::stages + st * L::stage_bytes;
                 mbar_arrive_expect_tx(B.full + st, L::k_bytes + L::v_bytes);
@@ -354,7 +360,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         if (lane == 0) {
             for (int t = 0; t < T; ++t) {
                 const int sv = t % L::NSV;
-                if (t >= L::NSV && !wait_bar(B.vempty + sv, ((t / L::NSV) - 1) & 1, s_abort, a.status)) break;
+                if (t >= L::NSV && !wait_bar(B.vempty + sv, ((t / L::NSV) - 1) & 1, s_abort, a.status, 256)) break;
                 const int kb = t < numkv ? QB - 1 - t : QB;
                 unsigned char *stg = smem + L::vring + sv * L::v_bytes;
                 mbar_arrive_expect_tx(B.vfull + sv, L::v_bytes);
@@ -368,36 +374,45 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, GATED ? 2 * DVP : DVP, false, true);
             constexpr uint32_t idesc_pv_half = idesc_bf16(128, DVP, false, true);
+            // The tensor pipe starves if this thread does much between MMAs, so the shared-
+            // memory descriptors are built once; a stage or K-step offset is added to the
+            // start-address field (address >> 4 in bits 0-13, below 2^14 in shared memory).
+            constexpr uint32_t kstride = L::split ? L::k_bytes : L::stage_bytes;  // K slot to K slot
+            constexpr uint32_t vstride = L::split ? L::v_bytes : L::stage_bytes;  // V slot to V slot
+            const uint64_t dq = sw128_desc(sbase, 16, 1024);
+            const uint64_t dk0 = sw128_desc(sbase + L::stages, 16, 1024);
+            const uint64_t dvraw0 = sw128_desc(sbase + (L::split ? L::vring : L::stages + L::k_bytes), kRegion, 1024);
+            const uint64_t dvc0 = sw128_desc(sbase + L::stages + L::vre, L::lbo_cplx, 1024);
+            const uint32_t tS = tmem + L::s_col0;
             bool ok = wait_bar(B.q, 0, s_abort, a.status);
             auto issue_pv = [&](int t) -> bool {
-                const int st = t % NS, sb = t & 1, sv = t % L::NSV;
-                if (!wait_bar(B.p_full + sb, (t >> 1) & 1, s_abort, a.status)) return false;
-                if (GATED && t < numkv && !wait_bar(B.vprep + st, (t / NS) & 1, s_abort, a.status))
+                const int st = t % NS, sb = t % L::NSB, sv = t % L::NSV;
+                if (!wait_bar(B.p_full + sb, (t / L::NSB) & 1, s_abort, a.status, 32)) return false;
+                if (GATED && t < numkv && !wait_bar(B.vprep + st, (t / NS) & 1, s_abort, a.status, 32))
                     return false;
-                if (L::split && !wait_bar(B.vfull + sv, (t / L::NSV) & 1, s_abort, a.status))
+                if (L::split && !wait_bar(B.vfull + sv, (t / L::NSV) & 1, s_abort, a.status, 32))
                     return false;
                 tc_fence_after();
-                const uint32_t stg = sbase + L::stages + st * L::stage_bytes;
-                // the raw V tile: in its own ring (g = 0) or behind K in the shared stage
-                const uint32_t vraw = L::split ? sbase + L::vring + sv * L::v_bytes : stg + L::k_bytes;
+                const uint32_t vslot = (uint32_t)(L::split ? sv : st);
+                const uint32_t acc0 = t > 0 ? 1u : 0u;
                 // P overwrites its own S buffer, except on the diagonal, whose P is written
                 // to the other buffer while its S is still being read
-                const uint32_t pcol = tmem + L::s_col0 + (t < numkv ? sb : (sb ^ 1)) * 128;
+                const uint32_t pcol = tS + (t < numkv ? sb : (t + 1) % L::NSB) * 128;
                 if (t < numkv) {
-                    const uint32_t vbase = GATED ? stg + L::vre : vraw;
-                    const uint32_t lbo = GATED ? L::lbo_cplx : kRegion;
+                    const uint64_t dv = (GATED ? dvc0 : dvraw0) + ((vslot * vstride) >> 4);
+                    umma_bf16_ts(tmem, pcol, dv, idesc_pv, acc0);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        umma_bf16_ts(tmem, pcol + ks * 8, sw128_desc(vbase + ks * 2048, lbo, 1024),
-                                     idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-                } else {  // diagonal tile: raw V, Re(P G) and Im(P G) from the two halves of S
+                    for (int ks = 1; ks < 8; ++ks)
+                        umma_bf16_ts(tmem, pcol + ks * 8, dv + (ks * 2048 >> 4), idesc_pv, 1u);
+                } else {  // diagonal tile: raw V, Re(P G) and Im(P G) from the two halves of P
+                    const uint64_t dv = dvraw0 + ((vslot * vstride) >> 4);
+                    umma_bf16_ts(tmem, pcol, dv, idesc_pv_half, acc0);
+                    if (GATED) umma_bf16_ts(tmem + DVP, pcol + 64, dv, idesc_pv_half, acc0);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t bd = sw128_desc(vraw + ks * 2048, kRegion, 1024);
-                        umma_bf16_ts(tmem, pcol + ks * 8, bd, idesc_pv_half, (t > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 1; ks < 8; ++ks) {
+                        umma_bf16_ts(tmem, pcol + ks * 8, dv + (ks * 2048 >> 4), idesc_pv_half, 1u);
                         if (GATED)
-                            umma_bf16_ts(tmem + DVP, pcol + 64 + ks * 8, bd, idesc_pv_half,
-                                         (t > 0 || ks > 0) ? 1u : 0u);
+                            umma_bf16_ts(tmem + DVP, pcol + 64 + ks * 8, dv + (ks * 2048 >> 4), idesc_pv_half, 1u);
                     }
                 }
                 umma_commit(B.pv_done + sb);
@@ -406,16 +421,15 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             };
             for (int t = 0; ok && t < T; ++t) {
                 const int nsk = L::split ? L::NSK : NS;  // stages of the ring that holds K
-                const int st = t % nsk, sb = t & 1;
-                if (!wait_bar(B.full + st, (t / nsk) & 1, s_abort, a.status)) { ok = false; break; }
-                if (t >= 2 && !wait_bar(B.pv_done + sb, ((t - 2) >> 1) & 1, s_abort, a.status)) { ok = false; break; }
+                const int st = t % nsk, sb = t % L::NSB;
+                if (!wait_bar(B.full + st, (t / nsk) & 1, s_abort, a.status, 32)) { ok = false; break; }
+                if (t >= L::NSB && !wait_bar(B.pv_done + sb, ((t / L::NSB) - 1) & 1, s_abort, a.status, 32)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t kst = sbase + L::stages + st * (L::split ? L::k_bytes : L::stage_bytes);
+                const uint64_t dk = dk0 + (((uint32_t)st * kstride) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < DP / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                    umma_bf16_ss(tmem + L::s_col0 + sb * 128, sw128_desc(sbase + off, 16, 1024),
-                                 sw128_desc(kst + off, 16, 1024), idesc_s, ks > 0);
+                    const uint32_t off = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
+                    umma_bf16_ss(tS + sb * 128, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(B.s_full + sb);
                 if (L::split) umma_commit(B.empty + st);  // the K stage is free once S is done
@@ -438,7 +452,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             // a wait that runs out sets the abort flag; the group leaves together after the
             // barrier below, so no thread is left waiting on it. (The stage being full also
             // means the softmax rows are done with this stage's previous |c_j|.)
-            wait_bar(B.full + st, (t / NS) & 1, s_abort, a.status);
+            wait_bar(B.full + st, (t / NS) & 1, s_abort, a.status, 128);
             const cplx c = key_scale(C, {sgv.x, sgv.y});
             const float rc = cabs(c);
             s_rc[st * 128 + j] = rc;
@@ -446,7 +460,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             if (*s_abort) break;
             s_alllive[st] = all;
             mbar_arrive(B.rc + st);  // the softmax rows need only |c_j|
-            if (L::alias) wait_bar(B.s_full + (t & 1), (t >> 1) & 1, s_abort, a.status);
+            if (L::alias) wait_bar(B.s_full + t % L::NSB, (t / L::NSB) & 1, s_abort, a.status, 64);
             // V'_j = c_j V_j: Re and Im halves, same swizzled position as V_j
             const uint32_t stg = sbase + L::stages + st * L::stage_bytes;
 #pragma unroll
@@ -487,9 +501,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         bool ok = true;
 
         for (int t = 0; t < numkv; ++t) {
-            const int st = t % NS, sb = t & 1;
+            const int st = t % NS, sb = t % L::NSB;
             const uint32_t scol = trow + L::s_col0 + sb * 128;
-            bool ready = wait_bar_warp(B.s_full + sb, (t >> 1) & 1, s_abort, a.status);
+            bool ready = wait_bar_warp(B.s_full + sb, (t / L::NSB) & 1, s_abort, a.status);
             if (GATED && ready) ready = wait_bar_warp(B.rc + st, (t / NS) & 1, s_abort, a.status);
             tc_fence_after();
             const float *rcs = s_rc + st * 128 + 64 * h;
@@ -536,10 +550,10 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             // the two halves exchange their maxima; the barrier also makes every S read of
             // this tile happen before either half writes P over it, and lets both halves
             // leave together if a wait ran out
-            s_hmax[(sb * 2 + h) * 128 + r] = mt;
+            s_hmax[((t & 1) * 2 + h) * 128 + r] = mt;
             ok = named_bar_and(kBarSoftmax, 256, ready && !*s_abort);
             if (!ok) break;
-            mt = fmaxf(mt, s_hmax[(sb * 2 + (h ^ 1)) * 128 + r]);
+            mt = fmaxf(mt, s_hmax[((t & 1) * 2 + (h ^ 1)) * 128 + r]);
             // move the maximum only when it grows by more than 2^8 (or is first set)
             float alpha = 1.f;
             if (mt > M2 + kRescaleLog2 || (M2 == -INFINITY && mt > -INFINITY)) {
@@ -549,7 +563,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             }
             if (h == 0 && __any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
                 // the accumulator holds P(<= t-1) V: wait for PV(t-1), then rescale
-                if (wait_bar_warp(B.pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, s_abort, a.status)) {
+                if (wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status)) {
                     tc_fence_after();
                     scale_acc_row(trow, L::acc_cols, t > 0 ? alpha : 1.f);
                 }
@@ -609,7 +623,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 
             // the row factor prefix_i, once every off-diagonal product is in the accumulator
             if (ok && GATED && numkv > 0) {
-                if (!wait_bar_warp(B.pv_done + ((numkv - 1) & 1), ((numkv - 1) >> 1) & 1, s_abort, a.status))
+                if (!wait_bar_warp(B.pv_done + (numkv - 1) % L::NSB, ((numkv - 1) / L::NSB) & 1, s_abort, a.status))
                     ok = false;
                 if (ok) {
                     tc_fence_after();
@@ -619,9 +633,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             }
 
             // diagonal tile: G_ij formed one gate at a time from j = i down
-            const int t = numkv, sb = t & 1;
+            const int t = numkv, sb = t % L::NSB;
             const uint32_t scol = trow + L::s_col0 + sb * 128;
-            if (ok && !wait_bar_warp(B.s_full + sb, (t >> 1) & 1, s_abort, a.status)) ok = false;
+            if (ok && !wait_bar_warp(B.s_full + sb, (t / L::NSB) & 1, s_abort, a.status)) ok = false;
             if (ok) {
                 tc_fence_after();
                 const int i = r;
@@ -653,14 +667,15 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 // P of the diagonal goes to the other S buffer, free once PV(t-1) is done
                 // (gated heads waited for it above, before the row factor)
                 if (!GATED && numkv > 0 &&
-                    !wait_bar_warp(B.pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, s_abort, a.status))
+                    !wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status))
                     ok = false;
                 if (ok && __any_sync(0xffffffffu, numkv > 0 && alpha != 1.f)) {
                     tc_fence_after();
                     scale_acc_row(trow, L::acc_cols, numkv > 0 ? alpha : 1.f);
                 }
             }
-            const uint32_t pdiag = trow + L::s_col0 + (sb ^ 1) * 128;
+            // (the buffer after this one: it last held P(t-2), or P(t-1) with two buffers)
+            const uint32_t pdiag = trow + L::s_col0 + ((t + 1) % L::NSB) * 128;
             if (ok) {
                 const int i = r;
                 cplx G = {1.f, 0.f};
@@ -711,7 +726,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             mbar_arrive(B.p_full + sb);
 
             // epilogue: O = acc e^{(1-beta) M} Z'^{-beta}
-            if (ok && !wait_bar_warp(B.pv_done + sb, (t >> 1) & 1, s_abort, a.status)) ok = false;
+            if (ok && !wait_bar_warp(B.pv_done + sb, (t / L::NSB) & 1, s_abort, a.status)) ok = false;
             if (ok) {
                 tc_fence_after();
                 bool bad = false;
