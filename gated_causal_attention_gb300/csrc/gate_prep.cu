@@ -174,8 +174,16 @@ __global__ void debug_path_product_kernel(const float2 *gate, const float2 *pref
     if (j <= i) {
         const int QB = i / kBlock, KB = j / kBlock;
         if (QB == KB) {
+            // as the head kernel forms it: a row of the upper half of the block reaches a key
+            // of the lower half through A_i = prod_{k=64..i} a_k, then one gate at a time
+            const int b0 = QB * kBlock, il = i - b0, jl = j - b0;
             cplx Gv = {1.f, 0.f};
-            for (int jj = i - 1; jj >= j; --jj) Gv = diag_step(Gv, {ga[jj + 1].x, ga[jj + 1].y});
+            int top = i;
+            if (il >= kBlock / 2 && jl < kBlock / 2) {
+                for (int k = b0 + kBlock / 2; k <= i; ++k) Gv = cmul(Gv, {ga[k].x, ga[k].y});
+                top = b0 + kBlock / 2 - 1;
+            }
+            for (int jj = top - 1; jj >= j; --jj) Gv = diag_step(Gv, {ga[jj + 1].x, ga[jj + 1].y});
             out = Gv;
         } else {
             cplx C = {1.f, 0.f};

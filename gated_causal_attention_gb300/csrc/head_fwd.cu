@@ -27,6 +27,9 @@
 // to stop, and the CTA winds down with its TMEM freed.
 #include "gate_products.cuh"
 
+#ifndef RS_PROD_FIRST
+#define RS_PROD_FIRST 1
+#endif
 namespace rs {
 
 namespace {
@@ -41,7 +44,9 @@ namespace {
 template <bool GATED>
 struct Roles {
     static constexpr int threads = GATED ? 512 : 384;
-    static constexpr int prod_wg = GATED ? 3 : 2;
+    static constexpr int prod_wg = RS_PROD_FIRST ? 0 : (GATED ? 3 : 2);
+    static constexpr int sm_wg0 = RS_PROD_FIRST ? 1 : 0;            // softmax: sm_wg0, sm_wg0 + 1
+    static constexpr int vprep_wg = RS_PROD_FIRST ? 3 : 2;
     static constexpr int launch_regs = GATED ? 128 : 168;
     static constexpr int softmax_regs = GATED ? 184 : 216;
     static constexpr int vprep_regs = 80;
@@ -82,7 +87,9 @@ struct Cfg {
     static constexpr uint32_t alllive = gm + 128 * 4;                 // int [NS]
     static constexpr uint32_t hmax = (alllive + NS * 4 + 15) & ~15u;  // float [2][2][128] half-row maxima
     static constexpr uint32_t zpart = hmax + 4 * 128 * 4;             // float [128] second half's Z'
-    static constexpr uint32_t bars = zpart + 128 * 4;                 // mbarriers
+    static constexpr uint32_t upA = zpart + 128 * 4;                  // float2 [128] prod a_{64..i}
+    static constexpr uint32_t upR = upA + 128 * 8;                    // float [128] prod |a_{64..i}|
+    static constexpr uint32_t bars = upR + 128 * 4;                   // mbarriers
     // q; full, empty, vprep, rc (4 each); s_full, p_full, pv_done (3 each); vfull, vempty (4 each)
     static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4;
     static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, numkv, abort
@@ -98,6 +105,7 @@ struct Cfg {
     static constexpr uint32_t lbo_cplx = alias ? (DVP == 64 ? k_bytes : kRegion) : kRegion;
     static_assert(split ? NSK >= 2 : NS >= 2, "shared memory too small for two stages");
     static_assert(end <= 227 * 1024 - 1024, "shared memory budget");
+    static_assert(end - small <= small_bytes, "small region budget");
     static_assert(acc_cols + NSB * 128 <= 512, "TMEM budget");
 };
 
@@ -117,6 +125,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     if (mbar_try_wait(addr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+#pragma unroll 1
         for (int i = 0; i < 32; ++i) {
             if (mbar_try_wait(addr, parity)) return true;
             if (sleep_ns) __nanosleep(sleep_ns);
@@ -170,6 +179,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
 // acc row <- alpha * acc row (ncols fp32 columns)
 __device__ __forceinline__ void scale_acc_row(uint32_t trow, int ncols, float alpha)
 {
+#pragma unroll 1
     for (int cc = 0; cc < ncols; cc += 32) {
         uint32_t r[32];
         RS_TMEM_LD32(trow + cc, r);
@@ -184,6 +194,7 @@ __device__ __forceinline__ void scale_acc_row(uint32_t trow, int ncols, float al
 // (acc_re + i acc_im) <- z * (acc_re + i acc_im)
 __device__ __forceinline__ void cscale_acc_row(uint32_t trow, int dvp, cplx z)
 {
+#pragma unroll 1
     for (int cc = 0; cc < dvp; cc += 32) {
         uint32_t re[32], im[32];
         RS_TMEM_LD32(trow + cc, re);
@@ -227,9 +238,11 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     int *s_alllive = reinterpret_cast<int *>(smem + L::alllive);
     float *s_hmax = reinterpret_cast<float *>(smem + L::hmax);  // [2 tiles][2 halves][128 rows]
     float *s_zpart = reinterpret_cast<float *>(smem + L::zpart);
+    float2 *s_upA = reinterpret_cast<float2 *>(smem + L::upA);
+    float *s_upR = reinterpret_cast<float *>(smem + L::upR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
-    const int kTmaWarp = RL::prod_wg * 4, kMmaWarp = RL::prod_wg * 4 + 1;
+    const int kTmaWarp = RL::prod_wg * 4, kMmaWarp = RL::prod_wg * 4 + 1, kPvWarp = RL::prod_wg * 4 + 2;
     const int n = a.n;
     const int nqt = (n + 127) / 128;
     const int QB = nqt - 1 - (int)(blockIdx.x / tab.count);
@@ -263,7 +276,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         tmem_relinquish();
     }
     // softmax threads (two per row: one per half of the key tile): the row factor prefix_i
-    const bool softmax = wg < 2;
+    const bool softmax = wg == RL::sm_wg0 || wg == RL::sm_wg0 + 1;
     const int r = tid & 127;  // query row (softmax) or key row (value prep)
     const int row = sQ + r;
     const bool valid = softmax && row < n;
@@ -279,11 +292,44 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             rq = 1.f;
         }
     }
-    if (GATED && wg == 2) {  // the query block's own gates, for the diagonal tile
+    if (GATED && wg == RL::vprep_wg) {  // the query block's own gates, for the diagonal tile
         float2 av = make_float2(0.f, 0.f);
         if (sQ + r < n) av = a.gate[tok0 + sQ + r];
         s_ga[r] = av;
         s_gm[r] = cabs({av.x, av.y});
+        if (r < 32) {
+            // rows of the upper half of the block: A_i = a_64 a_65 ... a_i (and its modulus
+            // product), so that keys of the lower half factor as A_i * prod_{k=j+1..63} a_k.
+            // Lane l holds rows 64 + 2l and 65 + 2l; a warp scan over the pair products.
+            const int i0 = 64 + 2 * r;
+            float2 g0 = make_float2(0.f, 0.f), g1 = make_float2(0.f, 0.f);
+            if (sQ + i0 < n) g0 = a.gate[tok0 + sQ + i0];
+            if (sQ + i0 + 1 < n) g1 = a.gate[tok0 + sQ + i0 + 1];
+            const cplx c0 = {g0.x, g0.y}, c1 = {g1.x, g1.y};
+            const float m0 = cabs(c0), m1 = cabs(c1);
+            cplx incl = cmul(c0, c1);
+            float rincl = m0 * m1;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const cplx y = shfl_up(incl, d);
+                const float ry = __shfl_up_sync(0xffffffffu, rincl, d);
+                if (r >= d) {
+                    incl = cmul(y, incl);
+                    rincl = ry * rincl;
+                }
+            }
+            cplx excl = shfl_up(incl, 1);
+            float rexcl = __shfl_up_sync(0xffffffffu, rincl, 1);
+            if (r == 0) {
+                excl = {1.f, 0.f};
+                rexcl = 1.f;
+            }
+            const cplx A0 = cmul(excl, c0);
+            s_upA[i0] = make_float2(A0.re, A0.im);
+            s_upA[i0 + 1] = make_float2(incl.re, incl.im);
+            s_upR[i0] = rexcl * m0;
+            s_upR[i0 + 1] = rincl;
+        }
     }
     tc_fence_before();
     const int rows_alive = __syncthreads_or(valid && rq > 0.f);
@@ -291,7 +337,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     const uint32_t tmem = *tmem_slot;
 
     // number of off-diagonal key tiles: stop at the first tile whose carry C is exactly 0
-    if (warp == RL::prod_wg * 4 + 2) {
+    if (warp == kPvWarp) {
         int numkv = rows_alive ? QB : 0;
         if (GATED && numkv > 0) {
             const float2 *T = a.carry + (int64_t)bh * nqt;
@@ -369,34 +415,55 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             }
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer: S = Q K^T
+        // A tcgen05.mma is accepted only about as fast as the tensor pipe retires the one
+        // before it, so an issuing thread that stops to wait leaves the pipe idle. S and PV
+        // therefore have a thread each: while one waits on its barriers the other issues.
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, GATED ? 2 * DVP : DVP, false, true);
-            constexpr uint32_t idesc_pv_half = idesc_bf16(128, DVP, false, true);
-            // The tensor pipe starves if this thread does much between MMAs, so the shared-
-            // memory descriptors are built once; a stage or K-step offset is added to the
-            // start-address field (address >> 4 in bits 0-13, below 2^14 in shared memory).
+            // descriptors built once; a stage or K-step offset is added to the start-address
+            // field (address >> 4 in bits 0-13, below 2^14 in shared memory)
             constexpr uint32_t kstride = L::split ? L::k_bytes : L::stage_bytes;  // K slot to K slot
-            constexpr uint32_t vstride = L::split ? L::v_bytes : L::stage_bytes;  // V slot to V slot
             const uint64_t dq = sw128_desc(sbase, 16, 1024);
             const uint64_t dk0 = sw128_desc(sbase + L::stages, 16, 1024);
+            const uint32_t tS = tmem + L::s_col0;
+            constexpr int nsk = L::split ? L::NSK : NS;  // stages of the ring that holds K
+            bool ok = wait_bar(B.q, 0, s_abort, a.status);
+            for (int t = 0; ok && t < T; ++t) {
+                const int st = t % nsk, sb = t % L::NSB;
+                if (!wait_bar(B.full + st, (t / nsk) & 1, s_abort, a.status, 32)) break;
+                // the S buffer last held P(t - NSB): its P V must be done
+                if (t >= L::NSB && !wait_bar(B.pv_done + sb, ((t / L::NSB) - 1) & 1, s_abort, a.status, 32)) break;
+                tc_fence_after();
+                const uint64_t dk = dk0 + (((uint32_t)st * kstride) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < DP / 16; ++ks) {
+                    const uint32_t off = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
+                    umma_bf16_ss(tS + sb * 128, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(B.s_full + sb);
+                if (L::split) umma_commit(B.empty + st);  // the K stage is free once S is done
+            }
+        }
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ MMA issuer: O += P V'
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = idesc_bf16(128, GATED ? 2 * DVP : DVP, false, true);
+            constexpr uint32_t idesc_pv_half = idesc_bf16(128, DVP, false, true);
+            constexpr uint32_t vstride = L::split ? L::v_bytes : L::stage_bytes;  // V slot to V slot
             const uint64_t dvraw0 = sw128_desc(sbase + (L::split ? L::vring : L::stages + L::k_bytes), kRegion, 1024);
             const uint64_t dvc0 = sw128_desc(sbase + L::stages + L::vre, L::lbo_cplx, 1024);
             const uint32_t tS = tmem + L::s_col0;
-            bool ok = wait_bar(B.q, 0, s_abort, a.status);
-            auto issue_pv = [&](int t) -> bool {
+            for (int t = 0; t < T; ++t) {
                 const int st = t % NS, sb = t % L::NSB, sv = t % L::NSV;
-                if (!wait_bar(B.p_full + sb, (t / L::NSB) & 1, s_abort, a.status, 32)) return false;
-                if (GATED && t < numkv && !wait_bar(B.vprep + st, (t / NS) & 1, s_abort, a.status, 32))
-                    return false;
-                if (L::split && !wait_bar(B.vfull + sv, (t / L::NSV) & 1, s_abort, a.status, 32))
-                    return false;
+                if (!wait_bar(B.p_full + sb, (t / L::NSB) & 1, s_abort, a.status, 32)) break;
+                if (GATED && t < numkv && !wait_bar(B.vprep + st, (t / NS) & 1, s_abort, a.status, 32)) break;
+                if (L::split && !wait_bar(B.vfull + sv, (t / L::NSV) & 1, s_abort, a.status, 32)) break;
                 tc_fence_after();
                 const uint32_t vslot = (uint32_t)(L::split ? sv : st);
                 const uint32_t acc0 = t > 0 ? 1u : 0u;
                 // P overwrites its own S buffer, except on the diagonal, whose P is written
-                // to the other buffer while its S is still being read
+                // to the next buffer while its S is still being read
                 const uint32_t pcol = tS + (t < numkv ? sb : (t + 1) % L::NSB) * 128;
                 if (t < numkv) {
                     const uint64_t dv = (GATED ? dvc0 : dvraw0) + ((vslot * vstride) >> 4);
@@ -417,28 +484,10 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 }
                 umma_commit(B.pv_done + sb);
                 umma_commit(L::split ? B.vempty + sv : B.empty + st);
-                return true;
-            };
-            for (int t = 0; ok && t < T; ++t) {
-                const int nsk = L::split ? L::NSK : NS;  // stages of the ring that holds K
-                const int st = t % nsk, sb = t % L::NSB;
-                if (!wait_bar(B.full + st, (t / nsk) & 1, s_abort, a.status, 32)) { ok = false; break; }
-                if (t >= L::NSB && !wait_bar(B.pv_done + sb, ((t / L::NSB) - 1) & 1, s_abort, a.status, 32)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t dk = dk0 + (((uint32_t)st * kstride) >> 4);
-#pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks) {
-                    const uint32_t off = ((ks >> 2) * kRegion + (ks & 3) * 32) >> 4;
-                    umma_bf16_ss(tS + sb * 128, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
-                }
-                umma_commit(B.s_full + sb);
-                if (L::split) umma_commit(B.empty + st);  // the K stage is free once S is done
-                if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
             }
-            if (ok) issue_pv(T - 1);
         }
     }
-    } else if (GATED && wg == 2) {
+    } else if (GATED && wg == RL::vprep_wg) {
         // ------------------------------------------------------------ value preparation
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RL::vprep_regs));
         const int j = r;
@@ -491,7 +540,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         // ------------------------------------------------------------ softmax rows
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RL::softmax_regs));
         // Two threads per query row: half h takes keys [64h, 64h + 64) of every key tile.
-        const int h = wg;
+        const int h = wg - RL::sm_wg0;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float scale2 = qk * 1.4426950408889634f / sqrtf((float)a.d);  // qk log2(e)/sqrt(d)
         const bool qk_on = qk != 0.f;
@@ -508,7 +557,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             tc_fence_after();
             const float *rcs = s_rc + st * 128 + 64 * h;
             // fast: every entry of every valid row of this warp is live (no masking needed)
-            const bool fast = __all_sync(0xffffffffu, !GATED || !ready || (s_alllive[st] && (rq > 0.f || !valid)));
+            const bool fast = !GATED || __all_sync(0xffffffffu, !ready || (s_alllive[st] && (rq > 0.f || !valid)));
             // this half's 64 logits stay in registers for both passes
             uint32_t s[64];
             if (qk_on && ready) {
@@ -519,21 +568,24 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             // pass 1: the half-row live maximum of t = qk s log2(e)
             float mt = -INFINITY;
             if (qk_on && fast) {
-                // max (or min, for qk < 0) of the raw logits, then one scaling;
-                // eight independent running extrema keep the dependency chains short
-                float hx[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) hx[e] = -INFINITY;
+                // max (or min, for qk < 0) of the raw logits, then one scaling; three-input
+                // extrema in four independent chains keep the dependency chains short
+                float hx[4];
                 if (scale2 >= 0.f) {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) hx[e & 7] = fmaxf(hx[e & 7], __uint_as_float(s[e]));
+                    for (int e = 0; e < 4; ++e) hx[e] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2)
+                        hx[(e >> 1) & 3] = max3f(hx[(e >> 1) & 3], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+                    mt = max3f(hx[0], hx[1], fmaxf(hx[2], hx[3])) * scale2;
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) hx[e & 7] = fmaxf(hx[e & 7], -__uint_as_float(s[e]));
+                    for (int e = 0; e < 4; ++e) hx[e] = INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2)
+                        hx[(e >> 1) & 3] = min3f(hx[(e >> 1) & 3], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+                    mt = min3f(hx[0], hx[1], fminf(hx[2], hx[3])) * scale2;
                 }
-                const float hm = fmaxf(fmaxf(fmaxf(hx[0], hx[1]), fmaxf(hx[2], hx[3])),
-                                       fmaxf(fmaxf(hx[4], hx[5]), fmaxf(hx[6], hx[7])));
-                mt = hm * fabsf(scale2);
             } else if (qk_on) {
 #pragma unroll
                 for (int e = 0; e < 64; ++e) {
@@ -570,141 +622,137 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             }
             // pass 2: P = 2^{t - M} on live entries (bf16, two per TMEM column), Z' += |c_j| P.
             // A row with no live entry yet keeps M = -inf; its logits are still checked.
-            const float nMx = (M2 == -INFINITY) ? 0.f : -M2;
-            float zp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums
+            // Rows past n take -inf as their shift, so that their P is 0 without a select.
+            const float nMx = !valid ? -INFINITY : (M2 == -INFINITY) ? 0.f : -M2;
+            const float2 sc2 = make_float2(scale2, scale2), nm2 = make_float2(nMx, nMx);
+            const float2 z2 = make_float2(0.f, 0.f);
+            float2 zp[2] = {z2, z2}, cp[2] = {z2, z2};  // partial sums, two lanes each
             uint32_t pk[32];
+            // paired fp32 instructions: the logit scaling, the finiteness check and the Z'
+            // sum each take one instruction per two keys
+            auto pair = [&](int e, float2 w2, bool masked) {
+                const int k = (e >> 1) & 1;
+                const float2 x2 = qk_on ? fma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                               sc2, nm2)
+                                        : nm2;
+                cp[k] = fma2(x2, z2, cp[k]);
+                float2 p2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                if (masked) {  // gated heads with dead keys or a dead row: live entries only
+                    if (!(rq * w2.x > 0.f)) p2.x = 0.f;
+                    if (!(rq * w2.y > 0.f)) p2.y = 0.f;
+                }
+                zp[k] = GATED ? fma2(w2, p2, zp[k]) : add2(zp[k], p2);
+                pk[e >> 1] = pack_bf16x2(p2.x, p2.y);
+            };
             if (fast) {
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
                     const float4 w4 = GATED ? *reinterpret_cast<const float4 *>(rcs + e)
                                             : make_float4(1.f, 1.f, 1.f, 1.f);
-                    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-                    float p[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float x = qk_on ? fmaf(__uint_as_float(s[e + k]), scale2, nMx) : nMx;
-                        cp[k] = fmaf(x, 0.f, cp[k]);
-                        p[k] = valid ? ex2_approx(x) : 0.f;
-                        zp[k] = GATED ? fmaf(wv[k], p[k], zp[k]) : zp[k] + p[k];
-                    }
-                    pk[e >> 1] = pack_bf16x2(p[0], p[1]);
-                    pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
+                    pair(e, make_float2(w4.x, w4.y), false);
+                    pair(e + 2, make_float2(w4.z, w4.w), false);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    float p2[2];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const float w = GATED ? rcs[e + k] : 1.f;
-                        const float x = qk_on ? fmaf(__uint_as_float(s[e + k]), scale2, nMx) : nMx;
-                        cp[k] = fmaf(x, 0.f, cp[k]);
-                        const bool live = valid && rq * w > 0.f;
-                        p2[k] = live ? ex2_approx(x) : 0.f;
-                        zp[k] = fmaf(w, p2[k], zp[k]);
-                    }
-                    pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                for (int e = 0; e < 64; e += 4) {
+                    const float4 w4 = *reinterpret_cast<const float4 *>(rcs + e);
+                    pair(e, make_float2(w4.x, w4.y), true);
+                    pair(e + 2, make_float2(w4.z, w4.w), true);
                 }
             }
             RS_TMEM_ST16(scol + 32 * h, pk);
             RS_TMEM_ST16(scol + 32 * h + 16, (pk + 16));
-            Zs += (zp[0] + zp[1]) + (zp[2] + zp[3]);
-            chk += (cp[0] + cp[1]) + (cp[2] + cp[3]);
+            Zs += (zp[0].x + zp[0].y) + (zp[1].x + zp[1].y);
+            chk += (cp[0].x + cp[0].y) + (cp[1].x + cp[1].y);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(B.p_full + sb);
         }
 
-        // the second half hands its partial sum to the first, which does the rest
-        if (h == 1) s_zpart[r] = Zs + chk;  // chk is 0, or NaN to refuse
-        ok = named_bar_and(kBarSoftmax, 256, ok && !*s_abort);
-        if (h == 0) {
-            Zs += s_zpart[r];
-
-            // the row factor prefix_i, once every off-diagonal product is in the accumulator
-            if (ok && GATED && numkv > 0) {
-                if (!wait_bar_warp(B.pv_done + (numkv - 1) % L::NSB, ((numkv - 1) / L::NSB) & 1, s_abort, a.status))
-                    ok = false;
-                if (ok) {
-                    tc_fence_after();
-                    cscale_acc_row(trow, DVP, pq);
-                    Zs *= rq;
-                }
-            }
-
-            // diagonal tile: G_ij formed one gate at a time from j = i down
+        // ------------------------------------------------ diagonal tile (both halves)
+        // Half h takes keys [64h, 64h + 64) again. G_ij is formed one gate at a time from
+        // the top of the half down; a row of the upper half starts the lower half's chain
+        // from A_i = prod_{k=64..i} a_k. P goes to the next S buffer, so that S can be read
+        // again in the second pass.
+        {
             const int t = numkv, sb = t % L::NSB;
             const uint32_t scol = trow + L::s_col0 + sb * 128;
-            if (ok && !wait_bar_warp(B.s_full + sb, (t / L::NSB) & 1, s_abort, a.status)) ok = false;
-            if (ok) {
-                tc_fence_after();
-                const int i = r;
-                float mt = -INFINITY;
-                {
-                    float R = 1.f;
+            const uint32_t pd = trow + L::s_col0 + ((t + 1) % L::NSB) * 128;
+            const int i = r, jtop = 64 * h + 63;
+            const int jstop = i < jtop ? i : jtop;  // a_{j+1} enters the product for j < jstop
+            const bool from_upper = GATED && h == 0 && i > 63;
+            bool ready = ok && wait_bar_warp(B.s_full + sb, (t / L::NSB) & 1, s_abort, a.status);
+            tc_fence_after();
+            // pass 1: live maximum over j <= i
+            float mt = -INFINITY;
+            if (ready) {
+                float R = from_upper ? s_upR[i] : 1.f;
+#pragma unroll 1
+                for (int c = 1; c >= 0; --c) {
+                    float sv[32];
+                    if (qk_on) tmem_ld32f(scol + 64 * h + 32 * c, sv);
 #pragma unroll
-                    for (int c = 3; c >= 0; --c) {
-                        float sv[32];
-                        if (qk_on) tmem_ld32f(scol + c * 32, sv);
-                        if (c <= warp) {
-#pragma unroll
-                            for (int e = 31; e >= 0; --e) {
-                                const int j = c * 32 + e;
-                                if (GATED && j < i) R *= s_gm[j + 1];
-                                const float t2 = qk_on ? sv[e] * scale2 : 0.f;
-                                const bool live = valid && j <= i && R > 0.f;
-                                mt = live ? fmaxf(mt, t2) : mt;
-                            }
-                        }
+                    for (int e = 31; e >= 0; --e) {
+                        const int j = 64 * h + 32 * c + e;
+                        if (GATED && j < jstop) R *= s_gm[j + 1];
+                        const float t2 = qk_on ? sv[e] * scale2 : 0.f;
+                        const bool live = valid && j <= i && R > 0.f;
+                        mt = live ? fmaxf(mt, t2) : mt;
                     }
                 }
-                float alpha = 1.f;
+            }
+            s_hmax[((t & 1) * 2 + h) * 128 + r] = mt;
+            ok = named_bar_and(kBarSoftmax, 256, ready && !*s_abort);
+            float alpha = 1.f;
+            if (ok) {
+                mt = fmaxf(mt, s_hmax[((t & 1) * 2 + (h ^ 1)) * 128 + r]);
                 if (mt > M2 + kRescaleLog2 || (M2 == -INFINITY && mt > -INFINITY)) {
                     alpha = (M2 == -INFINITY) ? 0.f : ex2_approx(M2 - mt);
                     M2 = mt;
                     Zs *= alpha;
                 }
-                // P of the diagonal goes to the other S buffer, free once PV(t-1) is done
-                // (gated heads waited for it above, before the row factor)
-                if (!GATED && numkv > 0 &&
-                    !wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status))
+                // the off-diagonal sums take the row factor |prefix_i| now; the diagonal
+                // entries below carry their own R
+                if (GATED) Zs *= rq;
+                // the accumulator holds every off-diagonal P V: it takes alpha and (gated) the
+                // row factor prefix_i; P of this tile goes to a buffer that P V(t-1) or
+                // P V(t-2) read, so both halves wait for P V(t-1)
+                if (numkv > 0 && !wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status))
                     ok = false;
-                if (ok && __any_sync(0xffffffffu, numkv > 0 && alpha != 1.f)) {
+                if (ok && h == 0 && numkv > 0) {
                     tc_fence_after();
-                    scale_acc_row(trow, L::acc_cols, numkv > 0 ? alpha : 1.f);
+                    if (GATED)
+                        cscale_acc_row(trow, DVP, cmul(pq, {alpha, 0.f}));
+                    else if (__any_sync(0xffffffffu, alpha != 1.f))
+                        scale_acc_row(trow, L::acc_cols, alpha);
                 }
             }
-            // (the buffer after this one: it last held P(t-2), or P(t-1) with two buffers)
-            const uint32_t pdiag = trow + L::s_col0 + ((t + 1) % L::NSB) * 128;
+            // pass 2: P = G 2^{t - M} on live entries, Re and Im halves (gated)
             if (ok) {
-                const int i = r;
-                cplx G = {1.f, 0.f};
-                float R = 1.f;
-#pragma unroll
-                for (int c = 3; c >= 0; --c) {
+                cplx G = from_upper ? cplx{s_upA[i].x, s_upA[i].y} : cplx{1.f, 0.f};
+                float R = from_upper ? s_upR[i] : 1.f;
+#pragma unroll 1
+                for (int c = 1; c >= 0; --c) {
                     float sv[32];
-                    if (qk_on) tmem_ld32f(scol + c * 32, sv);
+                    if (qk_on) tmem_ld32f(scol + 64 * h + 32 * c, sv);
                     uint32_t pre[16], pim[16];
                     float odd_re = 0.f, odd_im = 0.f;  // key j+1 of the pair (j, j+1)
 #pragma unroll
                     for (int e = 31; e >= 0; --e) {
-                        const int j = c * 32 + e;
-                        float pr = 0.f, pi = 0.f;
-                        if (c <= warp) {
-                            if (GATED && j < i) {
-                                const float2 an = s_ga[j + 1];
-                                G = diag_step(G, {an.x, an.y});
-                                R *= s_gm[j + 1];
-                            }
-                            const bool causal = valid && j <= i;
-                            const float x = qk_on ? fmaf(sv[e], scale2, -M2) : -M2;
-                            if (causal) chk = fmaf(x, 0.f, chk);
-                            const bool live = causal && R > 0.f;
-                            const float p = live ? ex2_approx(x) : 0.f;
-                            Zs = fmaf(R, p, Zs);
-                            pr = GATED ? G.re * p : p;
-                            pi = GATED ? G.im * p : 0.f;
+                        const int j = 64 * h + 32 * c + e;
+                        if (GATED && j < jstop) {
+                            const float2 an = s_ga[j + 1];
+                            G = diag_step(G, {an.x, an.y});
+                            R *= s_gm[j + 1];
                         }
+                        const bool causal = valid && j <= i;
+                        const float x = qk_on ? fmaf(sv[e], scale2, -M2) : -M2;
+                        if (causal) chk = fmaf(x, 0.f, chk);
+                        const bool live = causal && R > 0.f;
+                        const float p = live ? ex2_approx(x) : 0.f;
+                        Zs = GATED ? fmaf(R, p, Zs) : Zs + p;
+                        const float pr = GATED ? G.re * p : p;
+                        const float pi = GATED ? G.im * p : 0.f;
                         // pack (j, j+1): the pair completes at even j
                         if (e & 1) {
                             odd_re = pr;
@@ -714,17 +762,21 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                             pim[e >> 1] = pack_bf16x2(pi, odd_im);
                         }
                     }
-                    RS_TMEM_ST16(pdiag + c * 16, pre);
-                    if (GATED) RS_TMEM_ST16(pdiag + 64 + c * 16, pim);
+                    RS_TMEM_ST16(pd + 32 * h + 16 * c, pre);
+                    if (GATED) RS_TMEM_ST16(pd + 64 + 32 * h + 16 * c, pim);
                 }
                 tmem_st_wait();
                 tc_fence_before();
             }
-            // both halves arrive on p_full: the second half does so on behalf of no work
-            // (the count stays 256)
             mbar_arrive(B.p_full + sb);
-            mbar_arrive(B.p_full + sb);
+        }
 
+        // the second half hands its partial sum to the first, which does the rest
+        if (h == 1) s_zpart[r] = Zs + chk;  // chk is 0, or NaN to refuse
+        ok = named_bar_and(kBarSoftmax, 256, ok && !*s_abort);
+        if (h == 0) {
+            Zs += s_zpart[r];
+            const int t = numkv, sb = t % L::NSB;
             // epilogue: O = acc e^{(1-beta) M} Z'^{-beta}
             if (ok && !wait_bar_warp(B.pv_done + sb, (t / L::NSB) & 1, s_abort, a.status)) ok = false;
             if (ok) {
@@ -739,6 +791,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 float *ore = a.O_re + (tok0 + row) * (int64_t)a.dv;
                 float *oim = a.O_im + (tok0 + row) * (int64_t)a.dv;
                 const bool vec = (a.dv & 3) == 0;
+#pragma unroll 1
                 for (int cc = 0; cc < DVP; cc += 32) {
                     uint32_t re[32], im[32];
                     RS_TMEM_LD32(trow + cc, re);
