@@ -104,17 +104,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // 3-D view [heads, rows, cols] of a bf16 tensor; boxes of 64 columns x 128 rows x 1 head,
 // 128-byte swizzle, rows past `rows` read as zeros.
-bool make_tmap(CUtensorMap *m, const void *base, int cols, int rows, int heads)
+// [heads, rows, cols] row-major, 128-byte swizzled boxes of 128 rows x 128 bytes:
+// bf16 inputs (box 64 x 128) or fp32 outputs (box 32 x 128).
+bool make_tmap(CUtensorMap *m, const void *base, int cols, int rows, int heads, bool f32 = false)
 {
     auto fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)rows * cols * es};
+    cuuint32_t box[3] = {f32 ? 32u : 64u, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Workspace of resolvent_head_forward.
@@ -316,9 +320,15 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
             g_launches += 1;
             vs = vp;
         }
-        CUtensorMap tq, tk, tv;
-        if (!make_tmap(&tq, qs, DP, n, BH) || !make_tmap(&tk, ks, DP, n, BH) ||
-            !make_tmap(&tv, vs, DVP, n, BH))
+        HeadMaps maps;
+        std::memset(&maps, 0, sizeof(maps));
+        if (!make_tmap(&maps.q, qs, DP, n, BH) || !make_tmap(&maps.k, ks, DP, n, BH) ||
+            !make_tmap(&maps.v, vs, DVP, n, BH))
+            return RS_ERR_CUDA;
+        // the outputs go out by tensor-map stores when their rows are a multiple of 16 bytes
+        const bool tma_out = dv % 4 == 0;
+        if (tma_out && (!make_tmap(&maps.ore, O_re, dv, n, BH, true) ||
+                        !make_tmap(&maps.oim, O_im, dv, n, BH, true)))
             return RS_ERR_CUDA;
         for (const HeadTable &t : head_tabs) {
             GatePrepArgs ga{};
@@ -332,7 +342,8 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
             HeadArgs ha{};
             ha.n = n; ha.d = d; ha.dv = dv; ha.gate = gate; ha.prefix = prefix; ha.suffix = suffix;
             ha.carry = carry; ha.O_re = O_re; ha.O_im = O_im; ha.status = status_dev;
-            if (launch_head_fwd(ha, t, tq, tk, tv, DP, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
+            ha.tma_out = tma_out ? 1 : 0;
+            if (launch_head_fwd(ha, t, maps, DP, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
             ++g_launches;
         }
         prof_mark(s, 1);

@@ -106,6 +106,9 @@ struct Cfg {
     static_assert(split ? NSK >= 2 : NS >= 2, "shared memory too small for two stages");
     static_assert(end <= 227 * 1024 - 1024, "shared memory budget");
     static_assert(end - small <= small_bytes, "small region budget");
+    // the epilogue stages O in the K/V ring: Re and Im (gated) or Re and one zero chunk
+    static constexpr uint32_t ring_bytes = split ? NSK * k_bytes + NSV * v_bytes : NS * stage_bytes;
+    static_assert((GATED ? 2 * (DVP / 32) : DVP / 32 + 1) * kRegion <= ring_bytes, "epilogue staging");
     static_assert(acc_cols + NSB * 128 <= 512, "TMEM budget");
 };
 
@@ -215,8 +218,7 @@ __device__ __forceinline__ void cscale_acc_row(uint32_t trow, int dvp, cplx z)
 template <int DP, int DVP, bool GATED>
 __global__ void __launch_bounds__(Roles<GATED>::threads, 1)
 head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
-                const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv)
+                const __grid_constant__ HeadMaps maps)
 {
     using L = Cfg<DP, DVP, GATED>;
     using RL = Roles<GATED>;
@@ -263,13 +265,13 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         }
         *s_abort = 0;
         fence_mbar_init();
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
+        prefetch_tmap(&maps.q);
+        prefetch_tmap(&maps.k);
+        prefetch_tmap(&maps.v);
         // Q does not depend on anything the prologue works out: start it now
         mbar_arrive_expect_tx(B.q, L::q_bytes);
         for (int r = 0; r < DP / 64; ++r)
-            tma_load_3d(smem + r * kRegion, &tq, B.q, r * 64, sQ, bh);
+            tma_load_3d(smem + r * kRegion, &maps.q, B.q, r * 64, sQ, bh);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
@@ -386,7 +388,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 unsigned char *stg = smem + L::stages + st * L::k_bytes;
                 mbar_arrive_expect_tx(B.full + st, L::k_bytes);
                 for (int rr = 0; rr < DP / 64; ++rr)
-                    tma_load_3d(stg + rr * kRegion, &tk, B.full + st, rr * 64, kb * 128, bh);
+                    tma_load_3d(stg + rr * kRegion, &maps.k, B.full + st, rr * 64, kb * 128, bh);
             }
         } else if (lane == 0) {
             for (int t = 0; t < T; ++t) {
@@ -396,9 +398,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 unsigned char *stg = smem + L::stages + st * L::stage_bytes;
                 mbar_arrive_expect_tx(B.full + st, L::k_bytes + L::v_bytes);
                 for (int rr = 0; rr < DP / 64; ++rr)
-                    tma_load_3d(stg + rr * kRegion, &tk, B.full + st, rr * 64, kb * 128, bh);
+                    tma_load_3d(stg + rr * kRegion, &maps.k, B.full + st, rr * 64, kb * 128, bh);
                 for (int rr = 0; rr < DVP / 64; ++rr)
-                    tma_load_3d(stg + L::k_bytes + rr * kRegion, &tv, B.full + st, rr * 64, kb * 128, bh);
+                    tma_load_3d(stg + L::k_bytes + rr * kRegion, &maps.v, B.full + st, rr * 64, kb * 128, bh);
             }
         }
     } else if (L::split && warp == kTmaWarp + 3) {
@@ -411,7 +413,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 unsigned char *stg = smem + L::vring + sv * L::v_bytes;
                 mbar_arrive_expect_tx(B.vfull + sv, L::v_bytes);
                 for (int rr = 0; rr < DVP / 64; ++rr)
-                    tma_load_3d(stg + rr * kRegion, &tv, B.vfull + sv, rr * 64, kb * 128, bh);
+                    tma_load_3d(stg + rr * kRegion, &maps.v, B.vfull + sv, rr * 64, kb * 128, bh);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -771,59 +773,94 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             mbar_arrive(B.p_full + sb);
         }
 
-        // the second half hands its partial sum to the first, which does the rest
+        // the second half hands its partial sum to the first, which works out the output
+        // factor f = e^{(1-beta) M} Z'^{-beta} and the refusal; both halves then write O
         if (h == 1) s_zpart[r] = Zs + chk;  // chk is 0, or NaN to refuse
         ok = named_bar_and(kBarSoftmax, 256, ok && !*s_abort);
         if (h == 0) {
             Zs += s_zpart[r];
+            bool bad = false;
+            float f = 0.f;
+            if (valid) {
+                bad = isnan(chk) || !isfinite(M2) || !(Zs > 0.f) || !isfinite(Zs);
+                f = (beta == 0.f) ? exp2f(M2) : exp2f((1.f - beta) * M2 - beta * log2f(Zs));
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
+            s_zpart[r] = f;
+        }
+        // epilogue: every P V is in the accumulator once P V(diagonal) is done
+        {
             const int t = numkv, sb = t % L::NSB;
-            // epilogue: O = acc e^{(1-beta) M} Z'^{-beta}
-            if (ok && !wait_bar_warp(B.pv_done + sb, (t / L::NSB) & 1, s_abort, a.status)) ok = false;
-            if (ok) {
+            bool done = ok && wait_bar_warp(B.pv_done + sb, (t / L::NSB) & 1, s_abort, a.status);
+            done = named_bar_and(kBarSoftmax, 256, done);  // also publishes f
+            const float f = s_zpart[r];
+            constexpr int nq = DVP / 32;  // 32-column chunks; half h writes chunks [h nq/2, (h+1) nq/2)
+            if (done) {
                 tc_fence_after();
-                bool bad = false;
-                float f = 0.f;
-                if (valid) {
-                    bad = isnan(chk) || !isfinite(M2) || !(Zs > 0.f) || !isfinite(Zs);
-                    f = (beta == 0.f) ? exp2f(M2) : exp2f((1.f - beta) * M2 - beta * log2f(Zs));
-                }
-                if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
-                float *ore = a.O_re + (tok0 + row) * (int64_t)a.dv;
-                float *oim = a.O_im + (tok0 + row) * (int64_t)a.dv;
-                const bool vec = (a.dv & 3) == 0;
+                if (a.tma_out) {
+                    // stage 128 rows x 32 columns per chunk in the free K/V ring, 128-byte
+                    // swizzled as the tensor map expects, then store it with one bulk copy
+                    const uint32_t stage_re = sbase + L::stages;
+                    const uint32_t stage_im = stage_re + nq * kRegion;
 #pragma unroll 1
-                for (int cc = 0; cc < DVP; cc += 32) {
-                    uint32_t re[32], im[32];
-                    RS_TMEM_LD32(trow + cc, re);
-                    if (GATED) RS_TMEM_LD32(trow + DVP + cc, im);
-                    tmem_ld_wait();
-                    if (valid) {
-                        if (vec && cc + 32 <= a.dv) {
+                    for (int q = h * nq / 2; q < (h + 1) * nq / 2; ++q) {
+                        uint32_t re[32], im[32];
+                        RS_TMEM_LD32(trow + 32 * q, re);
+                        if (GATED) RS_TMEM_LD32(trow + DVP + 32 * q, im);
+                        tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                float4 vr, vi;
-                                float *pr = &vr.x, *pi = &vi.x;
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t off = q * kRegion + r * 128 + ((c ^ (r & 7)) << 4);
+                            uint32_t wr[4], wi[4];
 #pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    const float xr = __uint_as_float(re[e + k]);
-                                    const float xi = GATED ? __uint_as_float(im[e + k]) : 0.f;
-                                    pr[k] = (xr == 0.f) ? 0.f : xr * f;  // an exact 0 stays 0 (never 0 * inf)
-                                    pi[k] = (xi == 0.f) ? 0.f : xi * f;
+                            for (int k = 0; k < 4; ++k) {
+                                const float xr = __uint_as_float(re[4 * c + k]);
+                                wr[k] = __float_as_uint(xr == 0.f ? 0.f : xr * f);  // an exact 0 stays 0
+                                if (GATED) {
+                                    const float xi = __uint_as_float(im[4 * c + k]);
+                                    wi[k] = __float_as_uint(xi == 0.f ? 0.f : xi * f);
                                 }
-                                *reinterpret_cast<float4 *>(ore + cc + e) = vr;
-                                *reinterpret_cast<float4 *>(oim + cc + e) = vi;
                             }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (cc + e < a.dv) {
-                                    const float xr = __uint_as_float(re[e]);
-                                    const float xi = GATED ? __uint_as_float(im[e]) : 0.f;
-                                    ore[cc + e] = (xr == 0.f) ? 0.f : xr * f;
-                                    oim[cc + e] = (xi == 0.f) ? 0.f : xi * f;
-                                }
+                            sts128(stage_re + off, make_uint4(wr[0], wr[1], wr[2], wr[3]));
+                            if (GATED) sts128(stage_im + off, make_uint4(wi[0], wi[1], wi[2], wi[3]));
                         }
                     }
+                    if (!GATED) {  // Im O = 0: one zero chunk, stored nq times
+                        const uint32_t z = stage_im + (uint32_t)(h * 128 + r) * 64;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sts128(z + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            done = named_bar_and(kBarSoftmax, 256, done);
+            if (done && a.tma_out && h == 0 && r == 0) {
+                const uint32_t stage_re = sbase + L::stages;
+                const uint32_t stage_im = stage_re + nq * kRegion;
+                for (int q = 0; q < nq; ++q) {
+                    tma_store_3d(&maps.ore, stage_re + q * kRegion, 32 * q, sQ, bh);
+                    tma_store_3d(&maps.oim, GATED ? stage_im + q * kRegion : stage_im, 32 * q, sQ, bh);
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();  // the staging area must outlive the reads of the stores
+            }
+            if (done && !a.tma_out) {  // rows of dv % 4 != 0 floats: plain stores
+                float *ore = a.O_re + (tok0 + row) * (int64_t)a.dv;
+                float *oim = a.O_im + (tok0 + row) * (int64_t)a.dv;
+#pragma unroll 1
+                for (int q = h * nq / 2; q < (h + 1) * nq / 2; ++q) {
+                    uint32_t re[32], im[32];
+                    RS_TMEM_LD32(trow + 32 * q, re);  // warp-wide: every lane, valid row or not
+                    if (GATED) RS_TMEM_LD32(trow + DVP + 32 * q, im);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (valid && 32 * q + e < a.dv) {
+                            const float xr = __uint_as_float(re[e]);
+                            const float xi = GATED ? __uint_as_float(im[e]) : 0.f;
+                            ore[32 * q + e] = (xr == 0.f) ? 0.f : xr * f;
+                            oim[32 * q + e] = (xi == 0.f) ? 0.f : xi * f;
+                        }
                 }
             }
         }
@@ -839,8 +876,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 }
 
 template <int DP, int DVP, bool GATED>
-cudaError_t launch_t(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
-                     const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s)
+cudaError_t launch_t(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps, cudaStream_t s)
 {
     using L = Cfg<DP, DVP, GATED>;
     auto k = head_fwd_kernel<DP, DVP, GATED>;
@@ -853,31 +889,29 @@ cudaError_t launch_t(const HeadArgs &a, const HeadTable &tab, const CUtensorMap 
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
     if (e != cudaSuccess) return e;
     const int nqt = (a.n + 127) / 128;
-    k<<<nqt * tab.count, Roles<GATED>::threads, L::alloc, s>>>(a, tab, tq, tk, tv);
+    k<<<nqt * tab.count, Roles<GATED>::threads, L::alloc, s>>>(a, tab, maps);
     return cudaGetLastError();
 }
 
 template <bool GATED>
-cudaError_t launch_g(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
-                     const CUtensorMap &tk, const CUtensorMap &tv, int dpad, int dvpad,
+cudaError_t launch_g(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps, int dpad, int dvpad,
                      cudaStream_t s)
 {
-    if (dpad == 64 && dvpad == 64) return launch_t<64, 64, GATED>(a, tab, tq, tk, tv, s);
-    if (dpad == 64 && dvpad == 128) return launch_t<64, 128, GATED>(a, tab, tq, tk, tv, s);
-    if (dpad == 128 && dvpad == 64) return launch_t<128, 64, GATED>(a, tab, tq, tk, tv, s);
-    return launch_t<128, 128, GATED>(a, tab, tq, tk, tv, s);
+    if (dpad == 64 && dvpad == 64) return launch_t<64, 64, GATED>(a, tab, maps, s);
+    if (dpad == 64 && dvpad == 128) return launch_t<64, 128, GATED>(a, tab, maps, s);
+    if (dpad == 128 && dvpad == 64) return launch_t<128, 64, GATED>(a, tab, maps, s);
+    return launch_t<128, 128, GATED>(a, tab, maps, s);
 }
 
 }  // namespace
 
-cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
-                            const CUtensorMap &tk, const CUtensorMap &tv, int dpad, int dvpad,
+cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps, int dpad, int dvpad,
                             cudaStream_t s)
 {
     if (tab.count == 0 || a.n == 0) return cudaSuccess;
     // one launch serves heads of one kind: the caller splits gated and ungated heads
-    return tab.g[0] != 0.f ? launch_g<true>(a, tab, tq, tk, tv, dpad, dvpad, s)
-                           : launch_g<false>(a, tab, tq, tk, tv, dpad, dvpad, s);
+    return tab.g[0] != 0.f ? launch_g<true>(a, tab, maps, dpad, dvpad, s)
+                           : launch_g<false>(a, tab, maps, dpad, dvpad, s);
 }
 
 }  // namespace rs

@@ -78,11 +78,16 @@ struct HeadArgs {
     const float2 *gate, *prefix, *suffix, *carry;  // gate products of K1 (gated heads)
     float *O_re, *O_im;
     int32_t *status;
+    int tma_out;  // O_re / O_im written by tensor-map stores (dv % 4 == 0); else plain stores
+};
+// The tensor maps of one head launch: q, k, v (bf16, box 64 x 128) and, when tma_out is set,
+// O_re and O_im (fp32, box 32 x 128).
+struct HeadMaps {
+    CUtensorMap q, k, v, ore, oim;
 };
 // dpad, dvpad in {64, 128}
-cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const CUtensorMap &tq,
-                            const CUtensorMap &tk, const CUtensorMap &tv, int dpad, int dvpad,
-                            cudaStream_t s);
+cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps,
+                            int dpad, int dvpad, cudaStream_t s);
 
 // ---------------------------------------------------------------- debug path product
 cudaError_t launch_debug_path_product(const float2 *gate, const float2 *prefix,
