@@ -259,8 +259,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         for (int i = 0; i < L::nbars; ++i) {
             const uint64_t *b = bar0 + i;
             uint32_t count = 1;                                       // TMA / tcgen05.commit
-            if (b >= B.vprep && b < B.vprep + 8) count = 128;         // value-prep threads (vprep, rc)
-            if (b >= B.p_full && b < B.p_full + 3) count = 256;       // both softmax halves
+            if (b >= B.vprep && b < B.vprep + 8) count = 4;           // value-prep warps (vprep, rc)
+            if (b >= B.p_full && b < B.p_full + 3) count = 8;         // softmax warps, both halves
             mbar_init(bar0 + i, count);
         }
         *s_abort = 0;
@@ -510,7 +510,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             const bool all = named_bar_and(kBarVprep, 128, rc > 0.f);
             if (*s_abort) break;
             s_alllive[st] = all;
-            mbar_arrive(B.rc + st);  // the softmax rows need only |c_j|
+            // the softmax rows need only |c_j|; the barrier above ordered every warp's writes
+            if (lane == 0) mbar_arrive(B.rc + st);
             if (L::alias) wait_bar(B.s_full + t % L::NSB, (t / L::NSB) & 1, s_abort, a.status, 64);
             // V'_j = c_j V_j: Re and Im halves, same swizzled position as V_j
             const uint32_t stg = sbase + L::stages + st * L::stage_bytes;
@@ -535,7 +536,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(B.vprep + st);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.vprep + st);
             C = carry_step(C, {Tv.x, Tv.y});
         }
     } else if (softmax) {
@@ -668,7 +670,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             chk += (cp[0].x + cp[0].y) + (cp[1].x + cp[1].y);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(B.p_full + sb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.p_full + sb);  // one arrival per warp
         }
 
         // ------------------------------------------------ diagonal tile (both halves)
@@ -770,7 +773,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 tmem_st_wait();
                 tc_fence_before();
             }
-            mbar_arrive(B.p_full + sb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.p_full + sb);
         }
 
         // the second half hands its partial sum to the first, which works out the output
