@@ -3,6 +3,7 @@
 // resolvent_status_sync).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -343,6 +344,9 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
             ha.n = n; ha.d = d; ha.dv = dv; ha.gate = gate; ha.prefix = prefix; ha.suffix = suffix;
             ha.carry = carry; ha.O_re = O_re; ha.O_im = O_im; ha.status = status_dev;
             ha.tma_out = tma_out ? 1 : 0;
+            // about 24 MB of K and V per head group: a group's K/V tiles stay in L2
+            const size_t kv_head = (size_t)n * (DP + DVP) * 2;
+            ha.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / kv_head));
             if (launch_head_fwd(ha, t, maps, DP, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
             ++g_launches;
         }

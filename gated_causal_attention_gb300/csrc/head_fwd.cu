@@ -247,8 +247,14 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     const int kTmaWarp = RL::prod_wg * 4, kMmaWarp = RL::prod_wg * 4 + 1, kPvWarp = RL::prod_wg * 4 + 2;
     const int n = a.n;
     const int nqt = (n + 127) / 128;
-    const int QB = nqt - 1 - (int)(blockIdx.x / tab.count);
-    const int slot = (int)(blockIdx.x % tab.count);
+    // Blocks run head group by head group (the K/V of a group stays in L2 while its query
+    // tiles stream it), longest query tiles first within a group.
+    const int G = a.heads_per_group;
+    const int grp = (int)blockIdx.x / (G * nqt);
+    const int rem = (int)blockIdx.x - grp * G * nqt;
+    const int gsz = min(G, tab.count - grp * G);
+    const int QB = nqt - 1 - rem / gsz;
+    const int slot = grp * G + rem % gsz;
     const int bh = tab.bh[slot];
     const float beta = tab.beta[slot], qk = tab.qk[slot];
     const int sQ = QB * 128;

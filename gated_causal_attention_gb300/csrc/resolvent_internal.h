@@ -79,6 +79,7 @@ struct HeadArgs {
     float *O_re, *O_im;
     int32_t *status;
     int tma_out;  // O_re / O_im written by tensor-map stores (dv % 4 == 0); else plain stores
+    int heads_per_group;  // blocks are ordered head group by head group (1 <= it <= table count)
 };
 // The tensor maps of one head launch: q, k, v (bf16, box 64 x 128) and, when tma_out is set,
 // O_re and O_im (fp32, box 32 x 128).
