@@ -91,15 +91,20 @@ def dist_barrier(world):
 # ------------------------------------------------------------------ work accounting
 
 def live_entries(u_head, g):
-    """Structurally live causal entries of one head: sum_i (i - z_i + 1), z_i the last
-    position k <= i (k >= 1) whose blended magnitude is exactly 0 (0 if none)."""
+    """Causal entries (i, j) whose path modulus R_ij = prod_{k=j+1..i} m_k is nonzero in fp32,
+    the precision the kernel evaluates G in: no exact zero gate on the path and the product
+    at least the smallest fp32 subnormal (2^-149). Entries past it are exact zeros of the evaluation and
+    count as no work. Per row the live keys are a contiguous run ending at j = i."""
     u = np.asarray(u_head, dtype=np.float64)
     n = u.size
-    m_zero = ((1.0 - g) + g * u) <= 0.0
-    m_zero[0] = False  # a_0 is never read
-    idx = np.where(m_zero, np.arange(n), 0)
-    z = np.maximum.accumulate(idx)
-    return float(np.sum(np.arange(n) - z + 1))
+    m = np.clip((1.0 - g) + g * u, 0.0, 1.0)
+    m[0] = 1.0  # a_0 is never read
+    with np.errstate(divide="ignore"):
+        lg = np.where(m > 0.0, np.log2(np.maximum(m, 1e-300)), -1e9)
+    L = np.cumsum(lg)  # L[k] = sum_{t<=k} log2 m_t, non-increasing
+    # R_ij = 2^(L[i] - L[j]) >= 2^-149  <=>  -L[j] >= -L[i] - 149 (a suffix of j, -L ascending)
+    first = np.searchsorted(-L, -L - 149.0, side="left")
+    return float(np.sum(np.arange(n) - first + 1))
 
 
 def head_work(hi: W.HeadInputs):

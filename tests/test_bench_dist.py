@@ -60,3 +60,31 @@ def test_work_accounting_counts_structurally_live_entries():
     # g = 1: m = u; zero at k = 2 (k = 0 is never read): rows 0..4 see 1, 2, 1, 2, 3 entries
     assert bench.live_entries(u, 1.0) == 9.0
     assert bench.live_entries(u, 0.0) == 15.0  # g = 0: every gate is 1
+
+
+def test_work_accounting_stops_at_fp32_underflow():
+    import numpy as np
+    import bench
+    # m = 1/2 everywhere: R_ij = 2^-(i-j) is nonzero in fp32 down to 2^-149, so row i has
+    # min(i, 149) + 1 live keys
+    n = 400
+    u = np.full(n, 0.5)
+    want = sum(min(i, 149) + 1 for i in range(n))
+    assert bench.live_entries(u, 1.0) == float(want)
+    # brute force with fp32 products on random gates
+    r = np.random.default_rng(3)
+    u = r.uniform(0.3, 1.0, 300)
+    m = np.clip(u, 0.0, 1.0).astype(np.float32)
+    cnt = 0
+    for i in range(300):
+        R = np.float32(1.0)
+        for j in range(i, -1, -1):
+            if j < i:
+                R = np.float32(R * m[j + 1])
+            if R == 0:
+                break
+            cnt += 1
+    # fp32 rounding in the subnormal range can keep a product at 2^-149 for a few more keys
+    # than the exact product: the count is exact-arithmetic, so never above the fp32 one
+    got = bench.live_entries(u, 1.0)
+    assert got <= cnt and cnt - got <= 0.01 * cnt
