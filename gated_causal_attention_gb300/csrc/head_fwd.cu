@@ -64,13 +64,14 @@ struct Cfg {
     static constexpr uint32_t q_bytes = (DP / 64) * kRegion;
     static constexpr uint32_t k_bytes = (DP / 64) * kRegion;
     static constexpr uint32_t v_bytes = (DVP / 64) * kRegion;
-    // Gated: Re V' goes where K was (once S(t) is done) and Im V' replaces V, when K is at
-    // least as wide as V; otherwise Re V' replaces V and Im V' takes a region of its own.
-    static constexpr bool alias = DP >= DVP;
-    static constexpr uint32_t extra = (GATED && !alias) ? v_bytes : 0;
-    static constexpr uint32_t stage_bytes = k_bytes + v_bytes + extra;
     static constexpr uint32_t small_bytes = 8192;
     static constexpr uint32_t budget = 227 * 1024 - 1024 - small_bytes - q_bytes;
+    // Gated: Re V' replaces V in place and Im V' takes a region of its own when four such
+    // stages fit; otherwise (when K is at least as wide as V) Re V' goes where K was, once
+    // S(t) is done, and Im V' replaces V.
+    static constexpr bool alias = DP >= DVP && budget / (k_bytes + 2 * v_bytes) < 4;
+    static constexpr uint32_t extra = (GATED && !alias) ? v_bytes : 0;
+    static constexpr uint32_t stage_bytes = k_bytes + v_bytes + extra;
     static constexpr int NS = (budget / stage_bytes) >= 4 ? 4 : (int)(budget / stage_bytes);
     static constexpr uint32_t stages = q_bytes;                       // stage s at stages + s*stage_bytes
     // Heads with g = 0 keep K and V in separate rings instead: a K stage frees as soon as its
@@ -519,8 +520,10 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             // the softmax rows need only |c_j|; the barrier above ordered every warp's writes
             if (lane == 0) mbar_arrive(B.rc + st);
             if (L::alias) wait_bar(B.s_full + t % L::NSB, (t / L::NSB) & 1, s_abort, a.status, 64);
-            // V'_j = c_j V_j: Re and Im halves, same swizzled position as V_j
+            // V'_j = c_j V_j: Re and Im halves, same swizzled position as V_j; c_j rounded to
+            // bf16 once, each product rounded to bf16
             const uint32_t stg = sbase + L::stages + st * L::stage_bytes;
+            const uint32_t cre2 = pack_bf16x2(c.re, c.re), cim2 = pack_bf16x2(c.im, c.im);
 #pragma unroll
             for (int rr = 0; rr < DVP / 64; ++rr) {
 #pragma unroll
@@ -532,10 +535,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                     uint32_t ore[4], oim[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_bf16x2(w[e]);
-                        ore[e] = pack_bf16x2(f.x * c.re, f.y * c.re);
-                        oim[e] = pack_bf16x2(f.x * c.im, f.y * c.im);
+                    for (int e = 0; e < 4; ++e) {  // two keys' elements per bf16x2 multiply
+                        ore[e] = mul_bf16x2(w[e], cre2);
+                        oim[e] = mul_bf16x2(w[e], cim2);
                     }
                     sts128(stg + L::vre + off, make_uint4(ore[0], ore[1], ore[2], ore[3]));
                     sts128(stg + L::vim + off, make_uint4(oim[0], oim[1], oim[2], oim[3]));
