@@ -340,6 +340,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             s_upR[i0 + 1] = rincl;
         }
     }
+    // the key-tile counter's first 32 block totals, loaded before the barrier
+    float2 carry0 = make_float2(1.f, 0.f);
+    if (GATED && warp == kPvWarp && lane < QB) carry0 = a.carry[(int64_t)bh * nqt + QB - 1 - lane];
     tc_fence_before();
     const int rows_alive = __syncthreads_or(valid && rq > 0.f);
     tc_fence_after();
@@ -354,7 +357,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             for (int base = 0; base < QB; base += 32) {
                 const int t = base + lane;
                 cplx x = {1.f, 0.f};
-                if (t < QB) {
+                if (base == 0) {
+                    x = {carry0.x, carry0.y};
+                } else if (t < QB) {
                     const float2 v = T[QB - 1 - t];
                     x = {v.x, v.y};
                 }
@@ -502,11 +507,20 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         const int j = r;
         cplx C = {1.f, 0.f};
         const float2 *Tc = a.carry + (int64_t)bh * nqt;
+        // the suffix product of key j and the block total of the next key tile are loaded one
+        // tile ahead, so their latency hides behind the current tile's work
+        float2 sg_next = make_float2(0.f, 0.f), T_next = make_float2(0.f, 0.f);
+        if (numkv > 0) {
+            sg_next = a.suffix[tok0 + (QB - 1) * 128 + j];
+            T_next = Tc[QB - 1];
+        }
         for (int t = 0; t < numkv; ++t) {
             const int st = t % NS;
-            const int kb = QB - 1 - t;
-            const float2 sgv = a.suffix[tok0 + kb * 128 + j];
-            const float2 Tv = Tc[kb];
+            const float2 sgv = sg_next, Tv = T_next;
+            if (t + 1 < numkv) {
+                sg_next = a.suffix[tok0 + (QB - 2 - t) * 128 + j];
+                T_next = Tc[QB - 2 - t];
+            }
             // a wait that runs out sets the abort flag; the group leaves together after the
             // barrier below, so no thread is left waiting on it. (The stage being full also
             // means the softmax rows are done with this stage's previous |c_j|.)
@@ -707,7 +721,11 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 #pragma unroll
                     for (int e = 31; e >= 0; --e) {
                         const int j = 64 * h + 32 * c + e;
-                        if (GATED && j < jstop) R *= s_gm[j + 1];
+                        // branch-free steps (the factor loads do not wait on the chain)
+                        if (GATED) {
+                            const float Rn = R * s_gm[min(j + 1, 127)];
+                            R = j < jstop ? Rn : R;
+                        }
                         const float t2 = qk_on ? sv[e] * scale2 : 0.f;
                         const bool live = valid && j <= i && R > 0.f;
                         mt = live ? fmaxf(mt, t2) : mt;
@@ -753,10 +771,12 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 #pragma unroll
                     for (int e = 31; e >= 0; --e) {
                         const int j = 64 * h + 32 * c + e;
-                        if (GATED && j < jstop) {
-                            const float2 an = s_ga[j + 1];
-                            G = diag_step(G, {an.x, an.y});
-                            R *= s_gm[j + 1];
+                        if (GATED) {
+                            const float2 an = s_ga[min(j + 1, 127)];
+                            const cplx Gn = diag_step(G, {an.x, an.y});
+                            const float Rn = R * s_gm[min(j + 1, 127)];
+                            G = j < jstop ? Gn : G;
+                            R = j < jstop ? Rn : R;
                         }
                         const bool causal = valid && j <= i;
                         const float x = qk_on ? fmaf(sv[e], scale2, -M2) : -M2;
