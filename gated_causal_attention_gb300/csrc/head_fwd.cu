@@ -6,37 +6,41 @@
 //
 // One CTA owns one 128-row query tile QB of one head. Key tiles run from KB = QB-1 down to
 // 0 (the off-diagonal tiles), then the diagonal tile KB = QB. The CTA is warp-specialised
-// and software-pipelined:
-//   warp 8      TMA producer: Q once, then K and V tiles into an NS-stage ring;
-//   warp 9      MMA issuer (one thread): S(t) = Q K(t)^T into one of two TMEM S buffers,
-//               then O += P(t-1) V'(t-1) with P read from TMEM (it overwrites S);
-//   warps 0-3   softmax, thread i = query row i: live-masked running maximum M (moved
-//               only when it grows by more than 2^8, so the accumulator is rarely
-//               rescaled), P = 2^{t - M} packed to bf16 into TMEM, the shifted sum Z', the
-//               row factor prefix_i, the diagonal tile and the epilogue;
-//   warps 4-7   value preparation (gated heads), thread j = key row j: c_j = C * suffix_j,
-//               V'_j = c_j V_j as [Re | Im] bf16 halves for one MMA with N = 2 dv, and the
-//               carry C <- C * (block total) for the next key tile.
+// and software-pipelined (warpgroup 0 is the producer, 1 and 2 the softmax halves, 3 the
+// value preparation of gated heads):
+//   producer warp 0   TMA: Q once, then K and V tiles (one K+V ring for gated heads, a K
+//                     ring and a V ring for g = 0 heads);
+//   producer warp 1   issues S(t) = Q K(t)^T into one of 2-3 TMEM S buffers;
+//   producer warp 2   counts the key tiles, then issues O += P(t) V'(t) with P read from
+//                     TMEM (it overwrites S). Two issuers, because a tcgen05.mma is accepted
+//                     only about as fast as the pipe retires the previous one;
+//   softmax halves    two threads per query row, keys [0,64) and [64,128) of each tile:
+//                     live-masked running maximum M (moved only when it grows by more than
+//                     2^8, so the accumulator is rarely rescaled), P = 2^{t - M} packed to
+//                     bf16 into TMEM, the shifted sum Z', the row factor prefix_i, the
+//                     diagonal tile and the epilogue;
+//   value preparation thread j = key row j: c_j = C * suffix_j, V'_j = c_j V_j as [Re | Im]
+//                     bf16 halves for one MMA with N = 2 dv, and the carry C <- C * (block
+//                     total) for the next key tile.
 // Across blocks the path product factors as prefix_i * C * suffix_j (gate_products.cuh);
 // C only ever gains factors, so the key tiles beyond the first exactly-zero C are exactly
 // dead and are never loaded. Inside the diagonal tile G_ij is formed one gate at a time
-// from j = i down, and two MMAs accumulate Re(P G) V and Im(P G) V.
+// from the top of each half down (rows of the upper half start the lower half from
+// A_i = a_64 ... a_i), and two MMAs accumulate Re(P G) V and Im(P G) V.
 // Heads with g = 0 have G = 1: no gate products, no value preparation, a real accumulator.
+// The epilogue stages O in the freed K/V ring and writes it with tensor-map stores.
 //
 // Every wait is bounded: one that runs out raises RS_STATUS_TIMEOUT, tells the other roles
 // to stop, and the CTA winds down with its TMEM freed.
 #include "gate_products.cuh"
 
-#ifndef RS_PROD_FIRST
-#define RS_PROD_FIRST 1
-#endif
 namespace rs {
 
 namespace {
 
-// Warpgroup roles: 0 and 1 softmax (each query row has one thread in each: keys 0-63 and
-// 64-127 of every key tile), 2 value preparation (gated heads only), then the producer
-// warpgroup: its warp 0 loads by TMA, warp 1 issues the MMAs, warp 2 counts the key tiles.
+// Warpgroup roles: 0 the producer (warp 0 loads by TMA, warp 1 issues S, warp 2 counts the
+// key tiles and then issues P V), 1 and 2 softmax (each query row has one thread in each:
+// keys 0-63 and 64-127 of every key tile), 3 value preparation (gated heads only).
 // After the prologue the producer (and value-prep) warpgroups hand registers to the softmax
 // warpgroups (setmaxnreg); the shares add up to exactly what the launch provides:
 //   gated:   512 threads x 128 = 2 x 128 x 184 + 128 x 80 + 128 x 64
@@ -44,9 +48,9 @@ namespace {
 template <bool GATED>
 struct Roles {
     static constexpr int threads = GATED ? 512 : 384;
-    static constexpr int prod_wg = RS_PROD_FIRST ? 0 : (GATED ? 3 : 2);
-    static constexpr int sm_wg0 = RS_PROD_FIRST ? 1 : 0;            // softmax: sm_wg0, sm_wg0 + 1
-    static constexpr int vprep_wg = RS_PROD_FIRST ? 3 : 2;
+    static constexpr int prod_wg = 0;
+    static constexpr int sm_wg0 = 1;  // softmax: warpgroups 1 and 2
+    static constexpr int vprep_wg = 3;
     static constexpr int launch_regs = GATED ? 128 : 168;
     static constexpr int softmax_regs = GATED ? 184 : 216;
     static constexpr int vprep_regs = 80;
