@@ -108,15 +108,16 @@ def live_entries(u_head, g):
 
 
 def head_work(hi: W.HeadInputs):
-    """Algorithmic flops of the fused head kernel(s) for one call: per non-chain head,
-    live entries x (2 d [qk != 0] + 2 dv c), c = 2 with complex gates (g != 0), else 1."""
+    """Algorithmic flops of the fused head kernel(s) for one call: per head with qk != 0,
+    live entries x (2 d + 2 dv c), c = 2 with complex gates (g != 0), else 1. Heads with
+    qk = 0 run as O(n) chains (O_i = y_i Z_i^-beta) and count as chain tokens."""
     beta, qk, g = hi.switches_bh()
     flops, chain_tokens = 0.0, 0
     for h in range(hi.B * hi.H):
-        if qk[h] == 0.0 and beta[h] == 0.0:
+        if qk[h] == 0.0:
             chain_tokens += hi.n
             continue
-        per_entry = 2 * hi.d * (qk[h] != 0.0) + 2 * hi.dv * (2 if g[h] != 0.0 else 1)
+        per_entry = 2 * hi.d + 2 * hi.dv * (2 if g[h] != 0.0 else 1)
         flops += per_entry * (live_entries(hi.u[h], g[h]) if g[h] != 0.0
                               else hi.n * (hi.n + 1) / 2)
     return flops, chain_tokens

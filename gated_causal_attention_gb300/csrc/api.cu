@@ -86,7 +86,9 @@ std::vector<HeadTable> tables_for(const rs_switches &sw, int B, int H, Pred pred
     return out;
 }
 
-bool is_chain_head(const Sw &s) { return s.qk == 0.f && s.beta == 0.f; }
+// qk = 0: W_ij = G_ij / Z_i^beta with Z_i = sum_{j<=i} R_ij = m_i Z_{i-1} + 1, so
+// O_i = y_i Z_i^{-beta} with y the chain over V: an O(n) evaluation for any beta.
+bool is_chain_head(const Sw &s) { return s.qk == 0.f; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -149,7 +151,8 @@ HeadWs head_ws(int B, int H, int n, int d, int dv, rs_dtype dt)
 
 struct ChainWs {
     int *counter, *flags;
-    float2 *agg_a, *agg_y, *incl_y;
+    float2 *agg_a, *agg_y, *incl_y, *agg_z;
+    float *incl_z;
     size_t zero_bytes;
 };
 
@@ -168,12 +171,16 @@ ChainWs chain_ws(void *base, int slots, int n, int dv)
     w.agg_y = reinterpret_cast<float2 *>(p);
     p += up256(sizeof(float2) * chunks * dv);
     w.incl_y = reinterpret_cast<float2 *>(p);
+    p += up256(sizeof(float2) * chunks * dv);
+    w.agg_z = reinterpret_cast<float2 *>(p);
+    p += up256(sizeof(float2) * chunks);
+    w.incl_z = reinterpret_cast<float *>(p);
     return w;
 }
 
 rs_status run_chain(const std::vector<HeadTable> &tabs, const float *u, const float *theta,
                     const void *b, int b_is_bf16, int n, int dv, float *y_re, float *y_im,
-                    void *scratch, int32_t *status, cudaStream_t s, bool profile)
+                    void *scratch, int32_t *status, cudaStream_t s, bool profile, bool normalize = false)
 {
     for (size_t i = 0; i < tabs.size(); ++i) {
         const HeadTable &t = tabs[i];
@@ -184,6 +191,7 @@ rs_status run_chain(const std::vector<HeadTable> &tabs, const float *u, const fl
         a.u = u; a.theta = theta; a.b = b; a.b_is_bf16 = b_is_bf16; a.n = n; a.dv = dv;
         a.y_re = y_re; a.y_im = y_im; a.counter = w.counter; a.flags = w.flags;
         a.agg_a = w.agg_a; a.agg_y = w.agg_y; a.incl_y = w.incl_y; a.status = status;
+        a.normalize = normalize ? 1 : 0; a.agg_z = w.agg_z; a.incl_z = w.incl_z;
         a.wait_limit_ns = g_wait_limit_ns; a.withhold_chunk = g_chain_withhold;
         if (profile && i == 0) prof_mark(s, 0);
         e = launch_chain_scan(a, t, s);
@@ -356,7 +364,7 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
     // qk = 0 and beta = 0: W = G exactly, so O is the chain over V.
     if (!chain_tabs.empty()) {
         st = run_chain(chain_tabs, u, theta, v, f32 ? 0 : 1, n, dv, O_re, O_im, ws + w.chain,
-                       status_dev, s, head_tabs.empty());
+                       status_dev, s, head_tabs.empty(), true);
         if (st != RS_OK) return st;
     }
     return RS_OK;

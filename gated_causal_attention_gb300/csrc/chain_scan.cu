@@ -37,7 +37,7 @@ __device__ __forceinline__ float load_val<__nv_bfloat16>(const __nv_bfloat16 *p)
     return __bfloat162float(*p);
 }
 
-template <int CPL, typename BT>
+template <int CPL, typename BT, bool NORM>
 __global__ void __launch_bounds__(256)
 chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
 {
@@ -46,6 +46,10 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ cplx s_gate[kChainChunk];
     __shared__ cplx s_warpA[kWarps], s_exA[kWarps];
+    // the normaliser chain z_i = m_i z_{i-1} + 1 (qk = 0 readout): gate moduli, warp maps
+    __shared__ float s_m[kChainChunk];
+    __shared__ float s_wAz[kWarps], s_wYz[kWarps], s_exAz[kWarps], s_exYz[kWarps];
+    __shared__ float s_zin;
 
     const int dv = a.dv, n = a.n;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -87,6 +91,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     if (tid < kChainChunk) {
         const int t = s0 + tid;
         cplx at = {1.f, 0.f};
+        float mt = 1.f;
         if (tid < len) {
             const float uu = a.u[bh * n + t], th = a.theta[bh * n + t];
             const float m = fminf(fmaxf(fmaf(g, uu, 1.f - g), 0.f), 1.f);
@@ -95,9 +100,14 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
             float sn, cs;
             sincosf(tp, &sn, &cs);
             at = {m * cs, m * sn};
-            if (t == 0) at = {0.f, 0.f};  // y_0 = b_0: nothing flows in ahead of token 0
+            mt = m;
+            if (t == 0) {  // y_0 = b_0 and z_0 = 1: nothing flows in ahead of token 0
+                at = {0.f, 0.f};
+                mt = 0.f;
+            }
         }
         s_gate[tid] = at;
+        s_m[tid] = mt;
     }
     if (__syncthreads_or(bad) && tid == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
     __shared__ int s_loaded;
@@ -132,6 +142,18 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int c = 0; c < CPL; ++c)
             if (ch0 + c < dv) s_warpY[warp * dv + ch0 + c] = y[c];
         if (lane == 0) s_warpA[warp] = A;
+        if (NORM) {  // the same stretch of the real chain (every lane alike)
+            float Az = 1.f, Yz = 0.f;
+            for (int t = tok0; t < tok1; ++t) {
+                const float m = s_m[t];
+                Yz = fmaf(m, Yz, 1.f);
+                Az *= m;
+            }
+            if (lane == 0) {
+                s_wAz[warp] = Az;
+                s_wYz[warp] = Yz;
+            }
+        }
     }
     __syncthreads();
 
@@ -155,6 +177,18 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
             }
             eA = cmul(wA, eA);
         }
+        float eAz = 1.f, eYz = 0.f;
+        if (NORM) {
+            for (int w = 0; w < kWarps; ++w) {
+                if (lane == 0) {
+                    s_exAz[w] = eAz;
+                    s_exYz[w] = eYz;
+                }
+                eYz = fmaf(s_wAz[w], eYz, s_wYz[w]);
+                eAz *= s_wAz[w];
+            }
+        }
+        float zin = 0.f;
 
         const int64_t me = (int64_t)slot * nchunks + chunk;
         const bool publish = ticket != a.withhold_chunk;
@@ -168,6 +202,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c)
                     if (ch0 + c < dv) a.incl_y[me * dv + ch0 + c] = make_float2(eY[c].re, eY[c].im);
+                if (NORM && lane == 0) a.incl_z[me] = eYz;
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_gpu(a.flags + me, 2);
@@ -178,11 +213,13 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                 for (int c = 0; c < CPL; ++c)
                     if (ch0 + c < dv) a.agg_y[me * dv + ch0 + c] = make_float2(eY[c].re, eY[c].im);
                 if (lane == 0) a.agg_a[me] = make_float2(eA.re, eA.im);
+                if (NORM && lane == 0) a.agg_z[me] = make_float2(eAz, eYz);
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_gpu(a.flags + me, 1);
             }
-            // look back: acc maps y_end(p) to y_end(chunk-1)
+            // look back: acc maps y_end(p) to y_end(chunk-1) (and z likewise)
+            float accAz = 1.f, accYz = 0.f;
             cplx accA = {1.f, 0.f};
             cplx accY[CPL];
 #pragma unroll
@@ -207,6 +244,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                     if (lane == 0) flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
 #pragma unroll
                     for (int c = 0; c < CPL; ++c) yin[c] = accY[c];
+                    zin = accYz;
                     break;
                 }
                 if (f == 2) {
@@ -220,6 +258,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                         const cplx t = cmul(accA, yp);
                         yin[c] = {t.re + accY[c].re, t.im + accY[c].im};
                     }
+                    if (NORM) zin = fmaf(accAz, __ldcg(a.incl_z + other), accYz);
                     break;
                 }
                 const float2 pa = __ldcg(a.agg_a + other);
@@ -234,9 +273,15 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                     accY[c] = {t.re + accY[c].re, t.im + accY[c].im};
                 }
                 accA = cmul(accA, {pa.x, pa.y});
+                if (NORM) {
+                    const float2 pz = __ldcg(a.agg_z + other);
+                    accYz = fmaf(accAz, pz.y, accYz);
+                    accAz *= pz.x;
+                }
                 if (!cnonzero(accA)) {  // a closed gate: nothing earlier reaches this chunk
 #pragma unroll
                     for (int c = 0; c < CPL; ++c) yin[c] = accY[c];
+                    zin = accYz;
                     break;
                 }
             }
@@ -248,6 +293,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                         a.incl_y[me * dv + ch0 + c] =
                             make_float2(t.re + eY[c].re, t.im + eY[c].im);
                 }
+                if (NORM && lane == 0) a.incl_z[me] = fmaf(eAz, zin, eYz);
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_gpu(a.flags + me, 2);
@@ -256,6 +302,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
             if (ch0 + c < dv) s_yin[ch0 + c] = yin[c];
+        if (lane == 0) s_zin = zin;
     }
     __syncthreads();
 
@@ -275,16 +322,25 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         }
         float *yr = a.y_re + (bh * n + s0) * (int64_t)dv;
         float *yi = a.y_im + (bh * n + s0) * (int64_t)dv;
+        // qk = 0 readout: O_i = y_i z_i^{-beta}
+        const float beta = tab.beta[slot];
+        const bool scale_out = NORM && beta != 0.f;
+        float z = NORM ? fmaf(s_exAz[warp], s_zin, s_exYz[warp]) : 0.f;
         for (int t = tok0; t < tok1; ++t) {
             const cplx at = s_gate[t];
             float vr[CPL], vi[CPL];
+            float fz = 1.f;
+            if (scale_out) {
+                z = fmaf(s_m[t], z, 1.f);
+                fz = exp2f(-beta * log2f(z));
+            }
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const float bv = (ch0 + c < dv) ? load_val(sb + t * dv + ch0 + c) : 0.f;
                 y[c] = cmul(at, y[c]);
                 y[c].re += bv;
-                vr[c] = y[c].re;
-                vi[c] = y[c].im;
+                vr[c] = y[c].re * fz;
+                vi[c] = y[c].im * fz;
             }
             if (ch0 + CPL <= dv && (dv % CPL) == 0) {
                 if constexpr (CPL == 4) {
@@ -309,12 +365,12 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     }
 }
 
-template <int CPL, typename BT>
+template <int CPL, typename BT, bool NORM>
 cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 {
     const int nchunks = (a.n + kChainChunk - 1) / kChainChunk;
     const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (2 * kWarps + 1) * a.dv;
-    auto k = chain_scan_kernel<CPL, BT>;
+    auto k = chain_scan_kernel<CPL, BT, NORM>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<tab.count * nchunks, 256, smem, s>>>(a, tab);
@@ -355,15 +411,23 @@ size_t chain_scratch_bytes(int slots, int n, int dv)
     const size_t chunks = (size_t)slots * nchunks;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     return up(sizeof(int) * (chunks + 1)) + up(sizeof(float2) * chunks) +
-           2 * up(sizeof(float2) * chunks * (size_t)dv);
+           2 * up(sizeof(float2) * chunks * (size_t)dv) + up(sizeof(float2) * chunks) +
+           up(sizeof(float) * chunks);
+}
+
+template <bool NORM>
+cudaError_t launch_n(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
+{
+    if (a.dv <= 32) return a.b_is_bf16 ? launch_t<1, __nv_bfloat16, NORM>(a, tab, s) : launch_t<1, float, NORM>(a, tab, s);
+    if (a.dv <= 64) return a.b_is_bf16 ? launch_t<2, __nv_bfloat16, NORM>(a, tab, s) : launch_t<2, float, NORM>(a, tab, s);
+    return a.b_is_bf16 ? launch_t<4, __nv_bfloat16, NORM>(a, tab, s) : launch_t<4, float, NORM>(a, tab, s);
 }
 
 cudaError_t launch_chain_scan(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 {
     if (tab.count == 0 || a.n == 0) return cudaSuccess;
-    if (a.dv <= 32) return a.b_is_bf16 ? launch_t<1, __nv_bfloat16>(a, tab, s) : launch_t<1, float>(a, tab, s);
-    if (a.dv <= 64) return a.b_is_bf16 ? launch_t<2, __nv_bfloat16>(a, tab, s) : launch_t<2, float>(a, tab, s);
-    return a.b_is_bf16 ? launch_t<4, __nv_bfloat16>(a, tab, s) : launch_t<4, float>(a, tab, s);
+    // the normaliser chain is compiled only into the qk = 0 readout variant
+    return a.normalize ? launch_n<true>(a, tab, s) : launch_n<false>(a, tab, s);
 }
 
 }  // namespace rs

@@ -60,6 +60,11 @@ struct ChainArgs {
     float2 *agg_a;               // [slots * nchunks]
     float2 *agg_y;               // [slots * nchunks * dv]
     float2 *incl_y;              // [slots * nchunks * dv]
+    // normalize != 0: also run the real chain z_i = m_i z_{i-1} + 1 (z_i = sum_j R_ij) and
+    // write y_i z_i^{-beta} with beta per head from the table (the qk = 0 readout)
+    int normalize;
+    float2 *agg_z;               // [slots * nchunks]: (prod m, z from a zero carry)
+    float *incl_z;               // [slots * nchunks]: z at the end of the chunk
     int32_t *status;
     uint64_t wait_limit_ns;
     int withhold_chunk;          // test knob: this ticket never publishes (-1: none)

@@ -103,8 +103,10 @@ size_t resolvent_head_workspace_bytes(int B, int H, int n, int d, int dv, rs_dty
  * fused, batched over B*H heads, per-head switches). q, k [B,H,n,d] and v [B,H,n,dv] are
  * bf16 (dtype RS_BF16) or fp32 (RS_F32: rounded to bf16 into the workspace first);
  * u, theta fp32 [B,H,n]; O_re, O_im fp32 [B,H,n,dv]. The contractions run on the tensor
- * cores in bf16 with fp32 accumulation. Heads with qk = 0 and beta = 0 (W = G exactly)
- * are evaluated as the chain. Supported: 1 <= d <= 128 with d % 8 == 0, 1 <= dv <= 128.
+ * cores in bf16 with fp32 accumulation. Heads with qk = 0 are evaluated in O(n): then
+ * W_ij = G_ij / Z_i^beta with Z_i = sum_{j<=i} R_ij = m_i Z_{i-1} + 1, so O_i = y_i Z_i^-beta
+ * with y the chain over V (at beta = 0, W = G exactly and O = y).
+ * Supported: 1 <= d <= 128 with d % 8 == 0, 1 <= dv <= 128.
  * Refusals (RS_STATUS_NONFINITE): non-finite q, k, u, theta, g*theta, or a non-finite
  * logit qk*s_ij on an evaluated entry (every diagonal entry is evaluated, so any
  * non-finite q or k row is caught). Outputs past the range of fp32 read +-inf, not NaN.
