@@ -57,8 +57,8 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
 
     BT *sb = reinterpret_cast<BT *>(smem);                                     // [128][dv]
     cplx *s_warpY = reinterpret_cast<cplx *>(smem + sizeof(BT) * kChainChunk * dv);  // [8][dv]
-    cplx *s_exY = s_warpY + kWarps * dv;                                        // [8][dv]
-    cplx *s_yin = s_exY + kWarps * dv;                                          // [dv]
+    cplx *s_exY = s_warpY;  // the exclusive prefixes replace the warps' maps in place
+    cplx *s_yin = s_warpY + kWarps * dv;                                        // [dv]
 
     if (tid == 0) {
         s_ticket = atomicAdd(a.counter, 1);
@@ -67,8 +67,10 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     }
     __syncthreads();
     const int ticket = s_ticket;
-    const int slot = ticket / nchunks, chunk = ticket % nchunks;
-    if (slot >= tab.count) return;
+    // chunk-major tickets: the heads of a table advance side by side, so each head has few
+    // unresolved chunks in flight and look-backs stay short
+    const int slot = ticket % tab.count, chunk = ticket / tab.count;
+    if (chunk >= nchunks) return;
     const int64_t bh = tab.bh[slot];
     const float g = tab.g[slot];
     const int s0 = chunk * kChainChunk;
@@ -165,13 +167,13 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int c = 0; c < CPL; ++c) eY[c] = {0.f, 0.f};
         for (int w = 0; w < kWarps; ++w) {
             if (lane == 0) s_exA[w] = eA;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c)
-                if (ch0 + c < dv) s_exY[w * dv + ch0 + c] = eY[c];
             const cplx wA = s_warpA[w];
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
+                // each lane reads its channels of warp w's map, then overwrites them with the
+                // exclusive prefix
                 const cplx wY = (ch0 + c < dv) ? s_warpY[w * dv + ch0 + c] : cplx{0.f, 0.f};
+                if (ch0 + c < dv) s_exY[w * dv + ch0 + c] = eY[c];
                 const cplx t = cmul(wA, eY[c]);
                 eY[c] = {t.re + wY.re, t.im + wY.im};
             }
@@ -369,7 +371,7 @@ template <int CPL, typename BT, bool NORM>
 cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 {
     const int nchunks = (a.n + kChainChunk - 1) / kChainChunk;
-    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (2 * kWarps + 1) * a.dv;
+    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (kWarps + 1) * a.dv;
     auto k = chain_scan_kernel<CPL, BT, NORM>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
