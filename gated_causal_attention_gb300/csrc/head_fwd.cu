@@ -674,13 +674,25 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 zp[k] = GATED ? fma2(w2, p2, zp[k]) : add2(zp[k], p2);
                 pk[e >> 1] = pack_bf16x2(p2.x, p2.y);
             };
-            if (fast) {
+            if (fast && !GATED) {
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
-                    const float4 w4 = GATED ? *reinterpret_cast<const float4 *>(rcs + e)
-                                            : make_float4(1.f, 1.f, 1.f, 1.f);
-                    pair(e, make_float2(w4.x, w4.y), false);
-                    pair(e + 2, make_float2(w4.z, w4.w), false);
+                    pair(e, make_float2(1.f, 1.f), false);
+                    pair(e + 2, make_float2(1.f, 1.f), false);
+                }
+            } else if (fast) {
+                // |c_j| of this half: shared loads issued 32 keys ahead of their use
+                const uint32_t wa = smem_u32(rcs);
+#pragma unroll
+                for (int e0 = 0; e0 < 64; e0 += 32) {
+                    uint4 wq[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) wq[q] = lds128(wa + (e0 + 4 * q) * 4);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        pair(e0 + 4 * q, make_float2(__uint_as_float(wq[q].x), __uint_as_float(wq[q].y)), false);
+                        pair(e0 + 4 * q + 2, make_float2(__uint_as_float(wq[q].z), __uint_as_float(wq[q].w)), false);
+                    }
                 }
             } else {
 #pragma unroll
