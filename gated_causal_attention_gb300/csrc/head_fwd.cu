@@ -573,7 +573,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         const int h = wg - RL::sm_wg0;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float scale2 = qk * 1.4426950408889634f / sqrtf((float)a.d);  // qk log2(e)/sqrt(d)
-        const bool qk_on = qk != 0.f;
+        // heads with qk = 0 never come here: they run as chains (O(n) readout)
         float M2 = -INFINITY;  // (stale) running live maximum, log2 units (same in both halves)
         float Zs = 0.f;        // this half's sum of R 2^{t - M}
         float chk = 0.f;       // turns NaN if an evaluated logit is not finite
@@ -590,16 +590,43 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             const bool fast = !GATED || __all_sync(0xffffffffu, !ready || (s_alllive[st] && (rq > 0.f || !valid)));
             // this half's 64 logits stay in registers for both passes
             uint32_t s[64];
-            if (qk_on && ready) {
+            if (ready) {
                 RS_TMEM_LD32(scol + 64 * h, s);
                 RS_TMEM_LD32(scol + 64 * h + 32, (s + 32));
                 tmem_ld_wait();
             }
-            // pass 1: the half-row live maximum of t = qk s log2(e)
-            float mt = -INFINITY;
-            if (qk_on && fast) {
-                // max (or min, for qk < 0) of the raw logits, then one scaling; three-input
-                // extrema in four independent chains keep the dependency chains short
+            // gated heads with dead entries (c_j = 0, or a row whose prefix is 0): their logits
+            // are checked, then replaced by a value whose scaled logit is about -1e30, so that
+            // they neither move the maximum nor give a P above 0. (Their P V and Z' terms carry
+            // the factor c_j or prefix_i, which is 0, whatever P is.)
+            bool any_live = true;
+            if (GATED && !fast) {
+                const float dead = fminf(fmaxf(-1e30f / scale2, -3e38f), 3e38f);
+                const uint32_t wa = smem_u32(rcs);
+                float cpd = 0.f;
+                any_live = false;
+#pragma unroll
+                for (int e0 = 0; e0 < 64; e0 += 4) {
+                    const uint4 wq = lds128(wa + e0 * 4);
+                    const float w[4] = {__uint_as_float(wq.x), __uint_as_float(wq.y),
+                                        __uint_as_float(wq.z), __uint_as_float(wq.w)};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const bool live = rq * w[k] > 0.f;
+                        any_live |= live;
+                        if (!live) {
+                            cpd = fmaf(__uint_as_float(s[e0 + k]) * scale2, 0.f, cpd);
+                            s[e0 + k] = __float_as_uint(dead);
+                        }
+                    }
+                }
+                chk += cpd;
+            }
+            // pass 1: the half-row live maximum of t = qk s log2(e): max (or min, for qk < 0)
+            // of the raw logits, then one scaling; three-input extrema in four independent
+            // chains keep the dependency chains short
+            float mt;
+            {
                 float hx[4];
                 if (scale2 >= 0.f) {
 #pragma unroll
@@ -616,19 +643,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                         hx[(e >> 1) & 3] = min3f(hx[(e >> 1) & 3], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
                     mt = min3f(hx[0], hx[1], fminf(hx[2], hx[3])) * scale2;
                 }
-            } else if (qk_on) {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float t2 = __uint_as_float(s[e]) * scale2;
-                    mt = (rq * rcs[e] > 0.f) ? fmaxf(mt, t2) : mt;
-                }
-            } else {
-                bool any = fast;
-                if (!fast)
-                    for (int e = 0; e < 64 && !any; ++e) any = rq * rcs[e] > 0.f;
-                mt = any ? 0.f : -INFINITY;
             }
-            if (!valid) mt = -INFINITY;
+            if (!valid || !any_live) mt = -INFINITY;
             // the two halves exchange their maxima; the barrier also makes every S read of
             // this tile happen before either half writes P over it, and lets both halves
             // leave together if a wait ran out
@@ -650,7 +666,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                     scale_acc_row(trow, L::acc_cols, t > 0 ? alpha : 1.f);
                 }
             }
-            // pass 2: P = 2^{t - M} on live entries (bf16, two per TMEM column), Z' += |c_j| P.
+            // pass 2: P = 2^{t - M} (bf16, two per TMEM column), Z' += |c_j| P.
             // A row with no live entry yet keeps M = -inf; its logits are still checked.
             // Rows past n take -inf as their shift, so that their P is 0 without a select.
             const float nMx = !valid ? -INFINITY : (M2 == -INFINITY) ? 0.f : -M2;
@@ -660,27 +676,21 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             uint32_t pk[32];
             // paired fp32 instructions: the logit scaling, the finiteness check and the Z'
             // sum each take one instruction per two keys
-            auto pair = [&](int e, float2 w2, bool masked) {
+            auto pair = [&](int e, float2 w2) {
                 const int k = (e >> 1) & 1;
-                const float2 x2 = qk_on ? fma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
-                                               sc2, nm2)
-                                        : nm2;
+                const float2 x2 = fma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, nm2);
                 cp[k] = fma2(x2, z2, cp[k]);
-                float2 p2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
-                if (masked) {  // gated heads with dead keys or a dead row: live entries only
-                    if (!(rq * w2.x > 0.f)) p2.x = 0.f;
-                    if (!(rq * w2.y > 0.f)) p2.y = 0.f;
-                }
+                const float2 p2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
                 zp[k] = GATED ? fma2(w2, p2, zp[k]) : add2(zp[k], p2);
                 pk[e >> 1] = pack_bf16x2(p2.x, p2.y);
             };
-            if (fast && !GATED) {
+            if (!GATED) {
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
-                    pair(e, make_float2(1.f, 1.f), false);
-                    pair(e + 2, make_float2(1.f, 1.f), false);
+                    pair(e, make_float2(1.f, 1.f));
+                    pair(e + 2, make_float2(1.f, 1.f));
                 }
-            } else if (fast) {
+            } else {
                 // |c_j| of this half: shared loads issued 32 keys ahead of their use
                 const uint32_t wa = smem_u32(rcs);
 #pragma unroll
@@ -690,16 +700,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                     for (int q = 0; q < 8; ++q) wq[q] = lds128(wa + (e0 + 4 * q) * 4);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        pair(e0 + 4 * q, make_float2(__uint_as_float(wq[q].x), __uint_as_float(wq[q].y)), false);
-                        pair(e0 + 4 * q + 2, make_float2(__uint_as_float(wq[q].z), __uint_as_float(wq[q].w)), false);
+                        pair(e0 + 4 * q, make_float2(__uint_as_float(wq[q].x), __uint_as_float(wq[q].y)));
+                        pair(e0 + 4 * q + 2, make_float2(__uint_as_float(wq[q].z), __uint_as_float(wq[q].w)));
                     }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 64; e += 4) {
-                    const float4 w4 = *reinterpret_cast<const float4 *>(rcs + e);
-                    pair(e, make_float2(w4.x, w4.y), true);
-                    pair(e + 2, make_float2(w4.z, w4.w), true);
                 }
             }
             RS_TMEM_ST16(scol + 32 * h, pk);
@@ -733,7 +736,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 #pragma unroll 1
                 for (int c = 1; c >= 0; --c) {
                     float sv[32];
-                    if (qk_on) tmem_ld32f(scol + 64 * h + 32 * c, sv);
+                    tmem_ld32f(scol + 64 * h + 32 * c, sv);
 #pragma unroll
                     for (int e = 31; e >= 0; --e) {
                         const int j = 64 * h + 32 * c + e;
@@ -742,7 +745,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                             const float Rn = R * s_gm[min(j + 1, 127)];
                             R = j < jstop ? Rn : R;
                         }
-                        const float t2 = qk_on ? sv[e] * scale2 : 0.f;
+                        const float t2 = sv[e] * scale2;
                         const bool live = valid && j <= i && R > 0.f;
                         mt = live ? fmaxf(mt, t2) : mt;
                     }
@@ -781,7 +784,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 #pragma unroll 1
                 for (int c = 1; c >= 0; --c) {
                     float sv[32];
-                    if (qk_on) tmem_ld32f(scol + 64 * h + 32 * c, sv);
+                    tmem_ld32f(scol + 64 * h + 32 * c, sv);
                     uint32_t pre[16], pim[16];
                     float odd_re = 0.f, odd_im = 0.f;  // key j+1 of the pair (j, j+1)
 #pragma unroll
@@ -795,7 +798,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                             R = j < jstop ? Rn : R;
                         }
                         const bool causal = valid && j <= i;
-                        const float x = qk_on ? fmaf(sv[e], scale2, -M2) : -M2;
+                        const float x = fmaf(sv[e], scale2, -M2);
                         if (causal) chk = fmaf(x, 0.f, chk);
                         const bool live = causal && R > 0.f;
                         const float p = live ? ex2_approx(x) : 0.f;
