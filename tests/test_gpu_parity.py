@@ -290,3 +290,64 @@ def test_empty_sequence(R):
     zu = torch.zeros(1, 2, 0, device="cuda")
     Ore, Oim = R.head_forward(z, z, zu, zu, z, 1.0, 1.0, 0.5)
     assert Ore.shape == (1, 2, 0, 64) and Oim.numel() == 0
+
+
+# ------------------------------------------------------------------ qk = 0: the O(n) readout
+# With qk = 0 every live logit is 0, so W_ij = G_ij / Z_i^beta with Z_i = sum_{j<=i} R_ij,
+# and the library evaluates O_i = y_i Z_i^-beta with y the chain over V and
+# Z_i = m_i Z_{i-1} + 1. These cases check that rewrite against the oracle's dense
+# evaluation, and against closed forms that need no oracle.
+
+QK0_CASES = [
+    # n, dv, dtype, beta, g, u_range, zero_frac
+    (300, 64, "bf16", 0.5, 0.5, (0.5, 1.0), 0.03),
+    (1000, 5, "fp32", 1.0, 1.0, (0.0, 1.0), 0.02),
+    (257, 128, "bf16", 0.25, 0.0, (0.0, 1.0), 0.0),
+    (129, 16, "bf16", 0.75, 0.3, (-0.5, 1.5), 0.0),
+    (1, 64, "bf16", 1.0, 1.0, (0.0, 1.0), 0.0),
+]
+
+
+@pytest.mark.parametrize("case", QK0_CASES, ids=[str(i) for i in range(len(QK0_CASES))])
+def test_qk0_heads_match_oracle(R, oracle_mod, case):
+    n, dv, dt, beta, g, ur, zf = case
+    hi = W.head_inputs(1, 2, n, 64, dv, seed=900 + n + dv, dtype=dt, u_range=ur, zero_frac=zf,
+                       beta=beta, qk=0.0, g=g)
+    O = run_head(R, hi)
+    rows = np.arange(n)
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, str(case))
+
+
+def test_qk0_rows_are_stochastic(R):
+    """beta = 1, qk = 0, real gates (theta = 0): sum_j W_ij = 1 for every row, so V = 1 gives
+    O = 1 exactly up to rounding, with no imaginary part."""
+    n = 700
+    hi = W.head_inputs(1, 2, n, 64, 8, seed=41, u_range=(0.5, 1.0), zero_frac=0.02,
+                       theta_range=(0.0, 0.0), beta=1.0, qk=0.0, g=1.0)
+    hi.v[:] = 1.0
+    O = run_head(R, hi)
+    assert np.max(np.abs(O.real - 1.0)) <= 1e-5
+    assert np.all(O.imag == 0)
+
+
+def test_qk0_beta0_g0_is_the_prefix_sum(R):
+    """beta = 0, qk = 0, g = 0: W is the causal all-ones matrix and O_i = sum_{j<=i} V_j."""
+    n, dv = 1000, 32
+    hi = W.head_inputs(1, 1, n, 64, dv, seed=43, beta=0.0, qk=0.0, g=0.0)
+    O = run_head(R, hi)[0]
+    v = hi.v[0].astype(np.float64)
+    want = np.cumsum(v, axis=0)
+    env = np.cumsum(np.abs(v), axis=0)
+    assert np.all(np.abs(O.real - want) <= GATE_TOL * env)
+    assert np.all(O.imag == 0)
+
+
+@pytest.mark.parametrize("beta,g,ur", [(0.5, 0.3, (-0.5, 1.5)), (1.0, 0.0, (0.0, 1.0))])
+def test_qk0_long_sequence_sampled_rows(R, oracle_mod, beta, g, ur):
+    """n = 65536: the normaliser chain crosses 512 chunks of the single-pass scan."""
+    n = 65536
+    hi = W.head_inputs(1, 2, n, 64, 64, seed=47, u_range=ur, beta=beta, qk=0.0, g=g)
+    O = run_head(R, hi)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, n - 1],
+                                     np.random.default_rng(5).choice(n, 40, replace=False)]))
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, f"beta={beta} g={g}")
