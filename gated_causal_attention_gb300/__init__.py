@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.resolvent_chain_scan.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P, _P, _SZ,
                                            _P, _P]
         L.resolvent_chain_scan.restype = _I
+        L.resolvent_chain_scan_carry.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P, _P,
+                                                 _P, _P, _SZ, _P, _P]
+        L.resolvent_chain_scan_carry.restype = _I
         L.resolvent_chain_scan_noalloc.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P,
                                                    _P, _P]
         L.resolvent_chain_scan_noalloc.restype = _I
@@ -220,8 +223,12 @@ def chain_workspace_bytes(B, H, n, dv) -> int:
 
 
 def chain_scan(u, theta, g: Switch, b, *, out=None, workspace=None, status=None, stream=None,
-               sync: bool = True):
-    """y_0 = b_0, y_i = a_i y_{i-1} + b_i; b fp32 [B,H,n,dv]. Returns (y_re, y_im)."""
+               sync: bool = True, carry_in=None, carry_out=None):
+    """y_0 = b_0, y_i = a_i y_{i-1} + b_i; b fp32 [B,H,n,dv]. Returns (y_re, y_im).
+
+    carry_in / carry_out (complex64 [B,H,dv] on the device, optional): continue from y at the
+    end of a previous segment (then y_0 = a_0 y_{-1} + b_0) and receive y at token n-1
+    (resolvent_chain_scan_carry)."""
     u = _dev(u, "u", torch.float32)
     theta = _dev(theta, "theta", torch.float32)
     b = _dev(b, "b", torch.float32)
@@ -236,9 +243,23 @@ def chain_scan(u, theta, g: Switch, b, *, out=None, workspace=None, status=None,
     if workspace is None:
         workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
     st = status if status is not None else new_status(dev)
-    _raise(lib().resolvent_chain_scan(_ptr(u), _ptr(theta), sw, _ptr(b), B, H, n, dv,
-                                      _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
-                                      workspace.numel(), _ptr(st), _stream(stream)))
+    if carry_in is None and carry_out is None:
+        _raise(lib().resolvent_chain_scan(_ptr(u), _ptr(theta), sw, _ptr(b), B, H, n, dv,
+                                          _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
+                                          workspace.numel(), _ptr(st), _stream(stream)))
+    else:
+        def carry(c, name):
+            if c is None:
+                return None
+            if c.dtype != torch.complex64 or c.shape != (B, H, dv) or not c.is_contiguous() \
+                    or c.device != dev:
+                raise ResolventError(RS_ERR_SHAPE, f"{name}: complex64 [B,H,dv] on {dev}")
+            return ctypes.c_void_p(torch.view_as_real(c).data_ptr())
+        _raise(lib().resolvent_chain_scan_carry(_ptr(u), _ptr(theta), sw, _ptr(b), B, H, n, dv,
+                                                carry(carry_in, "carry_in"),
+                                                carry(carry_out, "carry_out"), _ptr(out[0]),
+                                                _ptr(out[1]), _ptr(workspace), workspace.numel(),
+                                                _ptr(st), _stream(stream)))
     if sync and status is None:
         status_sync(st, stream)
     return out

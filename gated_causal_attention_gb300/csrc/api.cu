@@ -180,7 +180,8 @@ ChainWs chain_ws(void *base, int slots, int n, int dv)
 
 rs_status run_chain(const std::vector<HeadTable> &tabs, const float *u, const float *theta,
                     const void *b, int b_is_bf16, int n, int dv, float *y_re, float *y_im,
-                    void *scratch, int32_t *status, cudaStream_t s, bool profile, bool normalize = false)
+                    void *scratch, int32_t *status, cudaStream_t s, bool profile, bool normalize = false,
+                    const float2 *carry_in = nullptr, float2 *carry_out = nullptr)
 {
     for (size_t i = 0; i < tabs.size(); ++i) {
         const HeadTable &t = tabs[i];
@@ -192,6 +193,7 @@ rs_status run_chain(const std::vector<HeadTable> &tabs, const float *u, const fl
         a.y_re = y_re; a.y_im = y_im; a.counter = w.counter; a.flags = w.flags;
         a.agg_a = w.agg_a; a.agg_y = w.agg_y; a.incl_y = w.incl_y; a.status = status;
         a.normalize = normalize ? 1 : 0; a.agg_z = w.agg_z; a.incl_z = w.incl_z;
+        a.carry_in = carry_in; a.carry_out = carry_out;
         a.wait_limit_ns = g_wait_limit_ns; a.withhold_chunk = g_chain_withhold;
         if (profile && i == 0) prof_mark(s, 0);
         e = launch_chain_scan(a, t, s);
@@ -396,6 +398,33 @@ rs_status resolvent_chain_scan(const float *u, const float *theta, rs_switches s
         return RS_ERR_WORKSPACE;
     return run_chain(tables_for(sw, B, H, [](const Sw &) { return true; }), u, theta, b, 0, n, dv,
                      y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), true);
+}
+
+rs_status resolvent_chain_scan_carry(const float *u, const float *theta, rs_switches sw,
+                                     const float *b, int B, int H, int n, int dv,
+                                     const float *carry_in, float *carry_out, float *y_re,
+                                     float *y_im, void *workspace, size_t workspace_bytes,
+                                     int32_t *status_dev, void *stream)
+{
+    g_launches = 0;
+    if (B < 0 || H < 0 || n < 0) return RS_ERR_SHAPE;
+    if ((size_t)B * H == 0 || n == 0) return RS_OK;
+    if (dv <= 0) return RS_ERR_SHAPE;
+    if (dv > 128) return RS_ERR_UNSUPPORTED;
+    rs_status st = check_switches(sw, H);
+    if (st != RS_OK) return st;
+    if (!u || !theta || !b || !y_re || !y_im || !status_dev) return RS_ERR_SHAPE;
+    for (const void *p : {(const void *)u, (const void *)theta, (const void *)b, (const void *)y_re,
+                          (const void *)y_im, (const void *)workspace, (const void *)carry_in,
+                          (const void *)carry_out})
+        if (p && !aligned16(p)) return RS_ERR_ALIGN;
+    if (!workspace || workspace_bytes < resolvent_chain_workspace_bytes(B, H, n, dv))
+        return RS_ERR_WORKSPACE;
+    // the tables hold at most kMaxSlots heads each; carries are indexed by (b, h) directly
+    return run_chain(tables_for(sw, B, H, [](const Sw &) { return true; }), u, theta, b, 0, n, dv,
+                     y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), true,
+                     false, reinterpret_cast<const float2 *>(carry_in),
+                     reinterpret_cast<float2 *>(carry_out));
 }
 
 rs_status resolvent_chain_scan_noalloc(const float *u, const float *theta, rs_switches sw,

@@ -103,7 +103,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
             sincosf(tp, &sn, &cs);
             at = {m * cs, m * sn};
             mt = m;
-            if (t == 0) {  // y_0 = b_0 and z_0 = 1: nothing flows in ahead of token 0
+            if (t == 0 && !a.carry_in) {  // y_0 = b_0 and z_0 = 1: nothing flows in ahead of token 0
                 at = {0.f, 0.f};
                 mt = 0.f;
             }
@@ -199,11 +199,22 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int c = 0; c < CPL; ++c) yin[c] = {0.f, 0.f};
 
         if (chunk == 0) {
-            // nothing before the first chunk: its resolved carry is its own map's offset
-            if (publish) {
+            // before the first chunk: the carry of the previous segment, or nothing
+            if (a.carry_in) {
 #pragma unroll
                 for (int c = 0; c < CPL; ++c)
-                    if (ch0 + c < dv) a.incl_y[me * dv + ch0 + c] = make_float2(eY[c].re, eY[c].im);
+                    if (ch0 + c < dv) {
+                        const float2 v = a.carry_in[bh * dv + ch0 + c];
+                        yin[c] = {v.x, v.y};
+                    }
+            }
+            if (publish) {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    const cplx t = cmul(eA, yin[c]);
+                    if (ch0 + c < dv)
+                        a.incl_y[me * dv + ch0 + c] = make_float2(t.re + eY[c].re, t.im + eY[c].im);
+                }
                 if (NORM && lane == 0) a.incl_z[me] = eYz;
                 __threadfence();
                 __syncwarp();
@@ -331,6 +342,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int t = tok0; t < tok1; ++t) {
             const cplx at = s_gate[t];
             float vr[CPL], vi[CPL];
+            const bool last = a.carry_out && s0 + t == n - 1;
             float fz = 1.f;
             if (scale_out) {
                 z = fmaf(s_m[t], z, 1.f);
@@ -343,6 +355,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                 y[c].re += bv;
                 vr[c] = y[c].re * fz;
                 vi[c] = y[c].im * fz;
+                if (last && ch0 + c < dv) a.carry_out[bh * dv + ch0 + c] = make_float2(y[c].re, y[c].im);
             }
             if (ch0 + CPL <= dv && (dv % CPL) == 0) {
                 if constexpr (CPL == 4) {

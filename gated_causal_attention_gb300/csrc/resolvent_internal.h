@@ -65,6 +65,11 @@ struct ChainArgs {
     int normalize;
     float2 *agg_z;               // [slots * nchunks]: (prod m, z from a zero carry)
     float *incl_z;               // [slots * nchunks]: z at the end of the chunk
+    // streaming: y at the end of the previous segment of each head (float2 [BH*dv], or
+    // null: y_0 = b_0) and y at token n-1 written out (float2 [BH*dv], or null); with a
+    // carry-in, token 0 takes its own gate, y_0 = a_0 y_{-1} + b_0
+    const float2 *carry_in;
+    float2 *carry_out;
     int32_t *status;
     uint64_t wait_limit_ns;
     int withhold_chunk;          // test knob: this ticket never publishes (-1: none)

@@ -137,6 +137,25 @@ rs_status resolvent_chain_scan(const float *u, const float *theta, rs_switches s
                                int32_t *status_dev, void *stream);
 
 /*
+ * The same chain over one segment of a longer sequence (the resolvent applied across calls,
+ * as the page's block summaries carry a prefix from block to block): carry_in holds, per head,
+ * y at the end of the previous segment, and then token 0 takes its own gate,
+ * y_0 = a_0 y_{-1} + b_0; carry_out receives y at token n-1. Both are interleaved complex
+ * fp32 [B,H,dv] (re, im pairs), device memory owned by the caller, 16-byte aligned; either
+ * may be NULL (no carry-in: y_0 = b_0 as in resolvent_chain_scan; no carry-out: nothing
+ * written). carry_out may not alias carry_in. Chaining segments S1, S2, ... with carry_out of
+ * one as carry_in of the next gives the chain of the concatenated sequence up to rounding.
+ * Other arguments, layout and errors are those of resolvent_chain_scan. This entry has no
+ * counterpart on the pages (they state the chain for one whole sequence).
+ */
+rs_status resolvent_chain_scan_carry(const float *u, const float *theta, rs_switches sw,
+                                     const float *b, int B, int H, int n, int dv,
+                                     const float *carry_in, float *carry_out,
+                                     float *y_re, float *y_im,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *status_dev, void *stream);
+
+/*
  * resolvent_chain_scan without a workspace argument: the same chain, with its scratch in a
  * fixed 8 MiB array of device memory inside this library. (The pages have no counterpart;
  * this entry exists for callers, not for the method.)

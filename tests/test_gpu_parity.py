@@ -351,3 +351,60 @@ def test_qk0_long_sequence_sampled_rows(R, oracle_mod, beta, g, ur):
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, n - 1],
                                      np.random.default_rng(5).choice(n, 40, replace=False)]))
     assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, f"beta={beta} g={g}")
+
+
+# ------------------------------------------------------------------ chain across segments
+
+
+@pytest.mark.parametrize("cuts,dv", [((128,), 64), ((384,), 16), ((500, 777), 5), ((1, 2, 999), 64)])
+def test_chain_segments_with_carries(R, oracle_mod, cuts, dv):
+    """A sequence cut into segments, each call continuing from the previous call's carry-out,
+    gives the chain of the whole sequence (checked against the oracle with its forward-error
+    envelope); the last carry-out is y at token n-1."""
+    B, H, n = 1, 3, 1000
+    r = np.random.default_rng(300 + dv + len(cuts))
+    b = r.standard_normal((B * H, n, dv)).astype(np.float32)
+    u = r.uniform(0.9, 1.0, (B * H, n)).astype(np.float32)
+    u[r.uniform(size=u.shape) < 0.01] = 0.0
+    th = r.uniform(-math.pi, math.pi, (B * H, n)).astype(np.float32)
+    gs = [1.0, 0.5, 0.0]
+    bounds = [0, *cuts, n]
+    parts = []
+    carry = None
+    for s0, s1 in zip(bounds[:-1], bounds[1:]):
+        m = s1 - s0
+        cout = torch.empty(B, H, dv, dtype=torch.complex64, device="cuda")
+        yr, yi = R.chain_scan(dev(u[:, s0:s1].reshape(B, H, m)), dev(th[:, s0:s1].reshape(B, H, m)), gs,
+                              dev(b[:, s0:s1].reshape(B, H, m, dv)), carry_in=carry, carry_out=cout)
+        parts.append((yr.cpu().double().numpy() + 1j * yi.cpu().double().numpy()).reshape(B * H, m, dv))
+        carry = cout
+    y = np.concatenate(parts, axis=1)
+    ref, env, st = oracle_mod.chain_heads(u, th, f32(gs), b)
+    assert np.all(st == 0)
+    check_chain(y, ref, env)
+    last = carry.cpu().numpy().astype(np.complex128).reshape(B * H, dv)
+    assert np.array_equal(last, y[:, -1, :].astype(np.complex64).astype(np.complex128))
+
+
+def test_chain_carry_in_alone_matches_prefixed_sequence(R):
+    """A carry-in c gives the same y as the sequence with one extra token in front whose
+    output is c (b = c there, gate closed), cut off."""
+    B, H, n, dv = 1, 2, 300, 32
+    r = np.random.default_rng(9)
+    b = r.standard_normal((B * H, n, dv)).astype(np.float32)
+    u = r.uniform(0.5, 1.0, (B * H, n)).astype(np.float32)
+    th = r.uniform(-math.pi, math.pi, (B * H, n)).astype(np.float32)
+    c = (r.standard_normal((B * H, dv)) + 1j * r.standard_normal((B * H, dv))).astype(np.complex64)
+    yr, yi = R.chain_scan(dev(u.reshape(B, H, n)), dev(th.reshape(B, H, n)), 1.0,
+                          dev(b.reshape(B, H, n, dv)),
+                          carry_in=torch.from_numpy(c.reshape(B, H, dv)).cuda())
+    y = (yr.cpu().double().numpy() + 1j * yi.cpu().double().numpy()).reshape(B * H, n, dv)
+    # token 0 continues from c: y_0 = a_0 c + b_0
+    m0 = np.clip(u[:, 0].astype(np.float64), 0, 1)
+    a0 = m0 * np.exp(1j * th[:, 0].astype(np.float64))
+    want0 = a0[:, None] * c.astype(np.complex128) + b[:, 0, :]
+    assert np.max(np.abs(y[:, 0, :] - want0)) <= 1e-5 * (np.max(np.abs(want0)) + 1.0)
+    # and later tokens follow the recurrence from there
+    a1 = np.clip(u[:, 1].astype(np.float64), 0, 1) * np.exp(1j * th[:, 1].astype(np.float64))
+    want1 = a1[:, None] * y[:, 0, :] + b[:, 1, :]
+    assert np.max(np.abs(y[:, 1, :] - want1)) <= 1e-5 * (np.max(np.abs(want1)) + 1.0)
