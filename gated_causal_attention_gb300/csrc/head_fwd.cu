@@ -32,11 +32,13 @@
 //
 // Every wait is bounded: one that runs out raises RS_STATUS_TIMEOUT, tells the other roles
 // to stop, and the CTA winds down with its TMEM freed.
-#include "gate_products.cuh"
+#include "head_common.cuh"
 
 namespace rs {
 
 namespace {
+
+using namespace head;
 
 // Warpgroup roles: 0 the producer (warp 0 loads by TMA, warp 1 issues S, warp 2 counts the
 // key tiles and then issues P V), 1 and 2 softmax (each query row has one thread in each:
@@ -59,8 +61,6 @@ struct Roles {
                       threads * launch_regs,
                   "register shares exceed the launch");
 };
-constexpr uint32_t kRegion = 128 * 128;   // one 128-row x 128-byte swizzled region (16 KB)
-constexpr float kRescaleLog2 = 8.f;       // keep a stale maximum while the excess stays below 2^8
 constexpr int kBarSoftmax = 1, kBarVprep = 2;
 
 template <int DP, int DVP, bool GATED>
@@ -121,104 +121,6 @@ struct Barriers {
     // full/empty: the K+V ring (gated heads) or the K ring (g = 0); vfull/vempty: the V ring
     uint64_t *q, *full, *empty, *vprep, *rc, *s_full, *p_full, *pv_done, *vfull, *vempty;
 };
-
-// Bounded wait on an mbarrier phase; also gives up when another role of this CTA (abort
-// flag) or another CTA (status word) reported a timeout.
-// Roles off the critical path pass sleep_ns > 0 and nap between polls, so that their
-// spinning does not take issue slots from the softmax warps sharing their SM sub-partition.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                         int32_t *status, uint32_t sleep_ns = 0)
-{
-    const uint32_t addr = smem_u32(bar);
-    if (mbar_try_wait(addr, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i) {
-            if (mbar_try_wait(addr, parity)) return true;
-            if (sleep_ns) __nanosleep(sleep_ns);
-        }
-        if (*abort) return false;
-        if (*reinterpret_cast<volatile int32_t *>(status) & RS_STATUS_TIMEOUT_BIT) {
-            *abort = 1;
-            return false;
-        }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            flag_status(status, RS_STATUS_TIMEOUT_BIT);
-            return false;
-        }
-    }
-}
-
-// The same, with one answer for the whole warp (the warp then stays converged for the
-// warp-wide tcgen05.ld / tcgen05.st that follow).
-__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                              int32_t *status)
-{
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status, 32));
-}
-
-__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    RS_TMEM_LD32(taddr, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-// acc row <- alpha * acc row (ncols fp32 columns)
-__device__ __forceinline__ void scale_acc_row(uint32_t trow, int ncols, float alpha)
-{
-#pragma unroll 1
-    for (int cc = 0; cc < ncols; cc += 32) {
-        uint32_t r[32];
-        RS_TMEM_LD32(trow + cc, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-        RS_TMEM_ST32(trow + cc, r);
-    }
-    tmem_st_wait();
-}
-
-// (acc_re + i acc_im) <- z * (acc_re + i acc_im)
-__device__ __forceinline__ void cscale_acc_row(uint32_t trow, int dvp, cplx z)
-{
-#pragma unroll 1
-    for (int cc = 0; cc < dvp; cc += 32) {
-        uint32_t re[32], im[32];
-        RS_TMEM_LD32(trow + cc, re);
-        RS_TMEM_LD32(trow + dvp + cc, im);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const cplx x = cmul(z, {__uint_as_float(re[e]), __uint_as_float(im[e])});
-            re[e] = __float_as_uint(x.re);
-            im[e] = __float_as_uint(x.im);
-        }
-        RS_TMEM_ST32(trow + cc, re);
-        RS_TMEM_ST32(trow + dvp + cc, im);
-    }
-    tmem_st_wait();
-}
 
 template <int DP, int DVP, bool GATED>
 __global__ void __launch_bounds__(Roles<GATED>::threads, 1)
