@@ -382,9 +382,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 tc_fence_after();
                 const uint32_t vslot = (uint32_t)(L::split ? sv : st);
                 const uint32_t acc0 = t > 0 ? 1u : 0u;
-                // P overwrites its own S buffer, except on the diagonal, whose P is written
-                // to the next buffer while its S is still being read
-                const uint32_t pcol = tS + (t < numkv ? sb : (t + 1) % L::NSB) * 128;
+                const uint32_t pcol = tS + sb * 128;  // P overwrites its own S buffer
                 if (t < numkv) {
                     const uint64_t dv = (GATED ? dvc0 : dvraw0) + ((vslot * vstride) >> 4);
                     umma_bf16_ts(tmem, pcol, dv, idesc_pv, acc0);
@@ -618,41 +616,42 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         }
 
         // ------------------------------------------------ diagonal tile (both halves)
-        // Half h takes keys [64h, 64h + 64) again. G_ij is formed one gate at a time from
-        // the top of the half down; a row of the upper half starts the lower half's chain
-        // from A_i = prod_{k=64..i} a_k. P goes to the next S buffer, so that S can be read
-        // again in the second pass.
+        // Half h takes keys [64h, 64h + 64) again; its 64 logits stay in registers for both
+        // passes, so P is written over S in place once both halves have read theirs. G_ij is
+        // formed one gate at a time from the top of the half down; a row of the upper half
+        // starts the lower half's chain from A_i = prod_{k=64..i} a_k. The accumulator's row
+        // factor is applied after pass 2, while the last off-diagonal P V drains.
         {
             const int t = numkv, sb = t % L::NSB;
             const uint32_t scol = trow + L::s_col0 + sb * 128;
-            const uint32_t pd = trow + L::s_col0 + ((t + 1) % L::NSB) * 128;
             const int i = r, jtop = 64 * h + 63;
             const int jstop = i < jtop ? i : jtop;  // a_{j+1} enters the product for j < jstop
             const bool from_upper = GATED && h == 0 && i > 63;
             bool ready = ok && wait_bar_warp(B.s_full + sb, (t / L::NSB) & 1, s_abort, a.status);
             tc_fence_after();
+            uint32_t s[64];
+            if (ready) {
+                RS_TMEM_LD32(scol + 64 * h, s);
+                RS_TMEM_LD32(scol + 64 * h + 32, (s + 32));
+                tmem_ld_wait();
+            }
             // pass 1: live maximum over j <= i
             float mt = -INFINITY;
             if (ready) {
                 float R = from_upper ? s_upR[i] : 1.f;
-#pragma unroll 1
-                for (int c = 1; c >= 0; --c) {
-                    float sv[32];
-                    tmem_ld32f(scol + 64 * h + 32 * c, sv);
 #pragma unroll
-                    for (int e = 31; e >= 0; --e) {
-                        const int j = 64 * h + 32 * c + e;
-                        // branch-free steps (the factor loads do not wait on the chain)
-                        if (GATED) {
-                            const float Rn = R * s_gm[min(j + 1, 127)];
-                            R = j < jstop ? Rn : R;
-                        }
-                        const float t2 = sv[e] * scale2;
-                        const bool live = valid && j <= i && R > 0.f;
-                        mt = live ? fmaxf(mt, t2) : mt;
+                for (int e = 63; e >= 0; --e) {
+                    const int j = 64 * h + e;
+                    // branch-free steps (the factor loads do not wait on the chain)
+                    if (GATED) {
+                        const float Rn = R * s_gm[min(j + 1, 127)];
+                        R = j < jstop ? Rn : R;
                     }
+                    const bool live = valid && j <= i && R > 0.f;
+                    mt = live ? fmaxf(mt, __uint_as_float(s[e]) * scale2) : mt;
                 }
             }
+            // the exchange also orders every S read of this tile before either half's P
             s_hmax[((t & 1) * 2 + h) * 128 + r] = mt;
             ok = named_bar_and(kBarSoftmax, 256, ready && !*s_abort);
             float alpha = 1.f;
@@ -666,27 +665,12 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 // the off-diagonal sums take the row factor |prefix_i| now; the diagonal
                 // entries below carry their own R
                 if (GATED) Zs *= rq;
-                // the accumulator holds every off-diagonal P V: it takes alpha and (gated) the
-                // row factor prefix_i; P of this tile goes to a buffer that P V(t-1) or
-                // P V(t-2) read, so both halves wait for P V(t-1)
-                if (numkv > 0 && !wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status))
-                    ok = false;
-                if (ok && h == 0 && numkv > 0) {
-                    tc_fence_after();
-                    if (GATED)
-                        cscale_acc_row(trow, DVP, cmul(pq, {alpha, 0.f}));
-                    else if (__any_sync(0xffffffffu, alpha != 1.f))
-                        scale_acc_row(trow, L::acc_cols, alpha);
-                }
-            }
-            // pass 2: P = G 2^{t - M} on live entries, Re and Im halves (gated)
-            if (ok) {
+                // pass 2: P = G 2^{t - M} on live entries: Re over columns [32h, 32h+32),
+                // Im (gated) over [64 + 32h, 64 + 32h + 32)
                 cplx G = from_upper ? cplx{s_upA[i].x, s_upA[i].y} : cplx{1.f, 0.f};
                 float R = from_upper ? s_upR[i] : 1.f;
-#pragma unroll 1
+#pragma unroll
                 for (int c = 1; c >= 0; --c) {
-                    float sv[32];
-                    tmem_ld32f(scol + 64 * h + 32 * c, sv);
                     uint32_t pre[16], pim[16];
                     float odd_re = 0.f, odd_im = 0.f;  // key j+1 of the pair (j, j+1)
 #pragma unroll
@@ -700,7 +684,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                             R = j < jstop ? Rn : R;
                         }
                         const bool causal = valid && j <= i;
-                        const float x = fmaf(sv[e], scale2, -M2);
+                        const float x = fmaf(__uint_as_float(s[32 * c + e]), scale2, -M2);
                         if (causal) chk = fmaf(x, 0.f, chk);
                         const bool live = causal && R > 0.f;
                         const float p = live ? ex2_approx(x) : 0.f;
@@ -716,10 +700,23 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                             pim[e >> 1] = pack_bf16x2(pi, odd_im);
                         }
                     }
-                    RS_TMEM_ST16(pd + 32 * h + 16 * c, pre);
-                    if (GATED) RS_TMEM_ST16(pd + 64 + 32 * h + 16 * c, pim);
+                    RS_TMEM_ST16(scol + 32 * h + 16 * c, pre);
+                    if (GATED) RS_TMEM_ST16(scol + 64 + 32 * h + 16 * c, pim);
                 }
                 tmem_st_wait();
+                // the accumulator holds every off-diagonal P V: it takes alpha and (gated) the
+                // row factor prefix_i, once the last of them is done
+                if (h == 0 && numkv > 0 && (GATED || __any_sync(0xffffffffu, alpha != 1.f))) {
+                    if (wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status)) {
+                        tc_fence_after();
+                        if (GATED)
+                            cscale_acc_row(trow, DVP, cmul(pq, {alpha, 0.f}));
+                        else
+                            scale_acc_row(trow, L::acc_cols, alpha);
+                    } else {
+                        ok = false;
+                    }
+                }
                 tc_fence_before();
             }
             __syncwarp();
