@@ -184,7 +184,8 @@ class Clocks:
 
 
 KERNEL_SOURCES = {"head_fwd_kernel": ["head_fwd.cu", "common.cuh", "gate_products.cuh"],
-                  "chain_scan_kernel": ["chain_scan.cu", "common.cuh"]}
+                  "chain_scan_kernel": ["chain_scan.cu", "common.cuh"],
+                  "operator_kernel": ["operator.cu", "common.cuh", "gate_products.cuh"]}
 
 
 def measured_traffic(kernel, workload):
@@ -255,6 +256,20 @@ def oracle_sample_chain(ci: W.ChainInputs, target_s: float):
     return tok / dt, tok, dt
 
 
+def oracle_sample_operator(hi: W.HeadInputs, target_s: float):
+    """The oracle's dense W of whole heads: entries per second."""
+    import oracle
+    oracle.build()
+    beta, qk, g = [np.asarray(x, np.float32).astype(np.float64) for x in hi.switches_bh()]
+    heads, t0 = 0, time.perf_counter()
+    while heads < hi.B * hi.H and (heads == 0 or time.perf_counter() - t0 < target_s):
+        oracle.operator(hi.q[heads], hi.k[heads], hi.u[heads], hi.theta[heads], beta[heads],
+                        qk[heads], g[heads])
+        heads += 1
+    dt = time.perf_counter() - t0
+    return heads * hi.n * hi.n / dt, heads * hi.n * hi.n, dt
+
+
 def cpu_cores():
     import oracle
     oracle.build()
@@ -283,8 +298,13 @@ def run_reference(args):
     inp = make_inputs(args)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup) * 2)
     is_chain = isinstance(inp, W.ChainInputs)
-    sample = (lambda: oracle_sample_chain(inp, per_step)) if is_chain else \
-        (lambda: oracle_sample_head(inp, per_step, seed=7))
+    is_op = args.workload == "operator"
+    if is_chain:
+        sample = lambda: oracle_sample_chain(inp, per_step)
+    elif is_op:
+        sample = lambda: oracle_sample_operator(inp, per_step)
+    else:
+        sample = lambda: oracle_sample_head(inp, per_step, seed=7)
     for _ in range(args.warmup):
         sample()
     rates, toks, secs = [], 0, 0.0
@@ -295,16 +315,20 @@ def run_reference(args):
         secs += s
     value = toks / secs
     cores = cpu_cores()
-    line = {"impl": "reference", "metric": "head tokens/s" if not is_chain else "chain tokens/s",
-            "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+    unit = "entries/s" if is_op else "tokens/s"
+    metric = ("chain tokens/s (B*H*n/s)" if is_chain else
+              "operator entries/s (B*H*n*n/s)" if is_op else "head tokens/s (B*H*n/s)")
+    line = {"impl": "reference", "metric": metric,
+            "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, workloads.py)", "config": config_of(args, inp, 1),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": ("whole heads of the chain" if is_chain else
+                                        "whole heads' W" if is_op else
                                         "seeded random rows of every head") +
-                             f", {toks} tokens in {secs:.1f} s"},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                             f", {toks} {'entries' if is_op else 'tokens'} in {secs:.1f} s"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -324,6 +348,7 @@ def run_ours(args):
 
     inp = make_inputs(args)
     is_chain = isinstance(inp, W.ChainInputs)
+    is_op = args.workload == "operator"
     shp = (inp.B, inp.H, inp.n)
     tdev = lambda x, s, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(
         device=device, dtype=dt)
@@ -337,6 +362,18 @@ def run_ours(args):
         tokens = inp.B * inp.H * inp.n
         work = tokens * chain_bytes_per_token(inp.dv)
         host_in = [inp.u, inp.theta, inp.b]
+    elif is_op:
+        q, k = tdev(inp.q, (*shp, inp.d), torch.bfloat16), tdev(inp.k, (*shp, inp.d), torch.bfloat16)
+        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
+        out = (torch.empty(*shp, inp.n, device=device), torch.empty(*shp, inp.n, device=device))
+        ws = torch.empty(max(1, R.operator_workspace_bytes(*shp, inp.d, torch.bfloat16)),
+                         dtype=torch.uint8, device=device)
+        step = lambda: R.operator(q, k, u, th, inp.beta, inp.qk, inp.g, out=out, workspace=ws,
+                                  status=status, sync=False)
+        tokens = inp.B * inp.H * inp.n * inp.n  # entries of W
+        # bytes: W written (8 B per entry); q, k read (2 B x d each per token); u, theta
+        work = tokens * 8 + inp.B * inp.H * inp.n * (4 * inp.d + 8)
+        host_in = [inp.q, inp.k, inp.u, inp.theta]
     else:
         dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
         q, k = tdev(inp.q, (*shp, inp.d), dt), tdev(inp.k, (*shp, inp.d), dt)
@@ -387,11 +424,12 @@ def run_ours(args):
 
     pk, pk_kind = peaks()
     kern = statistics.mean(kernel_ms) if kernel_ms else float("nan")
-    if is_chain:
+    if is_chain or is_op:
+        kname = "chain_scan_kernel" if is_chain else "operator_kernel"
         achieved = work / (kern / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"],
-                "traffic": measured_traffic("chain_scan_kernel", args.workload), "kernel": "chain_scan_kernel",
+                "traffic": measured_traffic(kname, args.workload), "kernel": kname,
                 "kernel_ms": kern, "peak_kind": pk_kind,
                 "algorithmic_bytes_per_launch": work}
     else:
@@ -406,7 +444,10 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         pinned = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in host_in]
-        if not is_chain and inp.dtype == "bf16":
+        if is_op:
+            pinned[0] = pinned[0].to(torch.bfloat16).pin_memory()
+            pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
+        elif not is_chain and inp.dtype == "bf16":
             pinned[0] = pinned[0].to(torch.bfloat16).pin_memory()
             pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
             pinned[2] = pinned[2].to(torch.bfloat16).pin_memory()
@@ -420,6 +461,11 @@ def run_ours(args):
                 uu, tt, bb = dv_in
                 o = R.chain_scan(uu.view(shp), tt.view(shp), inp.g, bb.view(*shp, inp.dv), out=out,
                                  workspace=ws, status=status, sync=False)
+            elif is_op:
+                qq, kk, uu, tt = dv_in
+                o = R.operator(qq.view(*shp, inp.d), kk.view(*shp, inp.d), uu.view(shp),
+                               tt.view(shp), inp.beta, inp.qk, inp.g, out=out, workspace=ws,
+                               status=status, sync=False)
             else:
                 qq, kk, vv, uu, tt = dv_in
                 o = R.head_forward(qq.view(*shp, inp.d), kk.view(*shp, inp.d), uu.view(shp),
@@ -440,24 +486,28 @@ def run_ours(args):
         torch.cuda.synchronize()
         e_ms = dist_max(a.elapsed_time(b2) / args.steps, world, device)
         R.status_sync(status)
-        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "entries/s" if is_op else "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, toks, secs = (oracle_sample_chain(inp, args.cpu_seconds) if is_chain
+                            else oracle_sample_operator(inp, args.cpu_seconds) if is_op
                             else oracle_sample_head(inp, args.cpu_seconds))
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+        cpu = {"value": rate, "unit": "entries/s" if is_op else "tokens/s", "cores": cpu_cores(),
+               "kind": "oracle",
                "sample": (f"{toks // inp.n} whole heads" if is_chain else
+                          f"{toks // (inp.n * inp.n)} whole heads' W" if is_op else
                           f"{toks // (inp.B * inp.H)} seeded random rows of each of the "
                           f"{inp.B * inp.H} heads") + f" ({toks} tokens, {secs:.1f} s)"}
 
     if rank == 0:
-        line = {"metric": ("chain tokens/s (B*H*n/s)" if is_chain else "head tokens/s (B*H*n/s)"),
-                "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        line = {"metric": ("chain tokens/s (B*H*n/s)" if is_chain else
+                           "operator entries/s (B*H*n*n/s)" if is_op else "head tokens/s (B*H*n/s)"),
+                "value": value, "unit": "entries/s" if is_op else "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32" if is_chain else ("bf16" if inp.dtype == "bf16" else "f32->bf16"),
+                "dtype": "f32" if (is_chain or is_op) else ("bf16" if inp.dtype == "bf16" else "f32->bf16"),
                 "data": "synthetic (seeded, workloads.py)",
                 "config": dict(config_of(args, inp, world), l2="flushed between timed steps"),
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,

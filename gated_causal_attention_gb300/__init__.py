@@ -71,6 +71,11 @@ def lib() -> ctypes.CDLL:
         L.resolvent_head_forward.argtypes = [_P, _P, _P, _P, _P, _Switches, _I, _I, _I, _I, _I, _I,
                                              _P, _P, _P, _SZ, _P, _P]
         L.resolvent_head_forward.restype = _I
+        L.resolvent_operator_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+        L.resolvent_operator_workspace_bytes.restype = _SZ
+        L.resolvent_operator.argtypes = [_P, _P, _P, _P, _Switches, _I, _I, _I, _I, _I, _P, _P, _P,
+                                         _SZ, _P, _P]
+        L.resolvent_operator.restype = _I
         L.resolvent_chain_workspace_bytes.argtypes = [_I, _I, _I, _I]
         L.resolvent_chain_workspace_bytes.restype = _SZ
         L.resolvent_chain_scan.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P, _P, _SZ,
@@ -218,6 +223,11 @@ def head_forward(q, k, u, theta, v, beta: Switch, qk: Switch, g: Switch, *, out=
     return out
 
 
+def operator_workspace_bytes(B, H, n, d, dtype: torch.dtype) -> int:
+    return int(lib().resolvent_operator_workspace_bytes(
+        B, H, n, d, RS_F32 if dtype == torch.float32 else RS_BF16))
+
+
 def chain_workspace_bytes(B, H, n, dv) -> int:
     return int(lib().resolvent_chain_workspace_bytes(B, H, n, dv))
 
@@ -260,6 +270,34 @@ def chain_scan(u, theta, g: Switch, b, *, out=None, workspace=None, status=None,
                                                 carry(carry_out, "carry_out"), _ptr(out[0]),
                                                 _ptr(out[1]), _ptr(workspace), workspace.numel(),
                                                 _ptr(st), _stream(stream)))
+    if sync and status is None:
+        status_sync(st, stream)
+    return out
+
+
+def operator(q, k, u, theta, beta: Switch, qk: Switch, g: Switch, *, out=None, workspace=None,
+             status=None, stream=None, sync: bool = True):
+    """W [B,H,n,n] complex64 (section "Object"); q, k [B,H,n,d] bf16 or fp32."""
+    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype:
+        raise ResolventError(RS_ERR_UNSUPPORTED, "q, k must both be bf16 or both fp32")
+    dt = RS_F32 if q.dtype == torch.float32 else RS_BF16
+    q, k = _dev(q, "q"), _dev(k, "k")
+    u = _dev(u, "u", torch.float32)
+    theta = _dev(theta, "theta", torch.float32)
+    B, H, n, d = q.shape
+    if k.shape != q.shape or u.shape != (B, H, n) or theta.shape != u.shape:
+        raise ResolventError(RS_ERR_SHAPE, "shape mismatch")
+    sw, keep = _switches(H, beta, qk, g)
+    dev = q.device
+    if out is None:
+        out = (torch.empty(B, H, n, n, device=dev), torch.empty(B, H, n, n, device=dev))
+    wsb = int(lib().resolvent_operator_workspace_bytes(B, H, n, d, dt))
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    st = status if status is not None else new_status(dev)
+    _raise(lib().resolvent_operator(_ptr(q), _ptr(k), _ptr(u), _ptr(theta), sw, B, H, n, d, dt,
+                                    _ptr(out[0]), _ptr(out[1]), _ptr(workspace), workspace.numel(),
+                                    _ptr(st), _stream(stream)))
     if sync and status is None:
         status_sync(st, stream)
     return out

@@ -372,6 +372,77 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
     return RS_OK;
 }
 
+size_t resolvent_operator_workspace_bytes(int B, int H, int n, int d, rs_dtype dtype)
+{
+    if (B <= 0 || H <= 0 || n <= 0 || d <= 0) return 0;
+    return head_ws(B, H, n, d, 64, dtype).total;
+}
+
+rs_status resolvent_operator(const void *q, const void *k, const float *u, const float *theta,
+                             rs_switches sw, int B, int H, int n, int d, rs_dtype dtype,
+                             float *W_re, float *W_im, void *workspace, size_t workspace_bytes,
+                             int32_t *status_dev, void *stream)
+{
+    g_launches = 0;
+    if (B < 0 || H < 0 || n < 0) return RS_ERR_SHAPE;
+    if ((size_t)B * H == 0 || n == 0) return RS_OK;
+    if (d <= 0) return RS_ERR_SHAPE;
+    if (d > 128 || d % 8 != 0) return RS_ERR_UNSUPPORTED;
+    if (dtype != RS_F32 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED;
+    rs_status st = check_switches(sw, H);
+    if (st != RS_OK) return st;
+    if (!q || !k || !u || !theta || !W_re || !W_im || !status_dev) return RS_ERR_SHAPE;
+    for (const void *p : {q, k, (const void *)u, (const void *)theta, (const void *)W_re,
+                          (const void *)W_im, (const void *)workspace})
+        if (!aligned16(p)) return RS_ERR_ALIGN;
+    const HeadWs w = head_ws(B, H, n, d, 64, dtype);
+    if (!workspace || workspace_bytes < w.total) return RS_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    const int BH = B * H, DP = pad64(d);
+    const bool f32 = dtype == RS_F32;
+    auto tabs = tables_for(sw, B, H, [](const Sw &s) { return s.g != 0.f; });
+    const auto plain = tables_for(sw, B, H, [](const Sw &s) { return s.g == 0.f; });
+    tabs.insert(tabs.end(), plain.begin(), plain.end());
+    float2 *gate = reinterpret_cast<float2 *>(ws + w.gate);
+    float2 *prefix = reinterpret_cast<float2 *>(ws + w.prefix);
+    float2 *suffix = reinterpret_cast<float2 *>(ws + w.suffix);
+    float2 *carry = reinterpret_cast<float2 *>(ws + w.carry);
+    const void *qs = q, *ks = k;
+    if (w.copy_qk) {
+        __nv_bfloat16 *qp = reinterpret_cast<__nv_bfloat16 *>(ws + w.qpad);
+        __nv_bfloat16 *kp = reinterpret_cast<__nv_bfloat16 *>(ws + w.kpad);
+        if (launch_pad_to_bf16(q, f32, (int64_t)BH * n, d, qp, DP, status_dev, f32, s) != cudaSuccess ||
+            launch_pad_to_bf16(k, f32, (int64_t)BH * n, d, kp, DP, status_dev, f32, s) != cudaSuccess)
+            return RS_ERR_CUDA;
+        g_launches += 2;
+        qs = qp;
+        ks = kp;
+    }
+    HeadMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!make_tmap(&maps.q, qs, DP, n, BH) || !make_tmap(&maps.k, ks, DP, n, BH)) return RS_ERR_CUDA;
+    for (const HeadTable &t : tabs) {
+        if (t.g[0] == 0.f) continue;  // G = 1: no gate products
+        GatePrepArgs ga{};
+        ga.u = u; ga.theta = theta; ga.n = n; ga.gate = gate; ga.prefix = prefix;
+        ga.suffix = suffix; ga.carry = carry; ga.status = status_dev; ga.write_ungated = 0;
+        if (launch_gate_prep(ga, t, s) != cudaSuccess) return RS_ERR_CUDA;
+        ++g_launches;
+    }
+    prof_mark(s, 0);
+    for (const HeadTable &t : tabs) {
+        HeadArgs ha{};
+        ha.n = n; ha.d = d; ha.dv = 64; ha.gate = gate; ha.prefix = prefix; ha.suffix = suffix;
+        ha.carry = carry; ha.status = status_dev;
+        if (launch_operator(ha, t, maps, DP, W_re, W_im, s) != cudaSuccess) return RS_ERR_CUDA;
+        ++g_launches;
+    }
+    prof_mark(s, 1);
+    return RS_OK;
+}
+
 size_t resolvent_chain_workspace_bytes(int B, int H, int n, int dv)
 {
     if (B <= 0 || H <= 0 || n <= 0 || dv <= 0) return 0;

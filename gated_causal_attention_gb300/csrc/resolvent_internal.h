@@ -99,6 +99,9 @@ struct HeadMaps {
 // dpad, dvpad in {64, 128}
 cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps,
                             int dpad, int dvpad, cudaStream_t s);
+// The materialised operator W [n, n] (operator.cu): one launch per table of heads of one kind.
+cudaError_t launch_operator(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps, int dpad,
+                            float *W_re, float *W_im, cudaStream_t s);
 
 // ---------------------------------------------------------------- debug path product
 cudaError_t launch_debug_path_product(const float2 *gate, const float2 *prefix,

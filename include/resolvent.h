@@ -118,6 +118,25 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *status_dev, void *stream);
 
+/* Workspace bytes resolvent_operator needs for these sizes (0 when n == 0). */
+size_t resolvent_operator_workspace_bytes(int B, int H, int n, int d, rs_dtype dtype);
+
+/*
+ * The operator itself, section "Object" (Rust API `operator`): W_ij = G_ij e^{qk s_ij} / Z_i^beta
+ * for every head, with the log-domain normaliser and the refusals of section "Evaluation and
+ * refusals". q, k [B,H,n,d] bf16 (RS_BF16) or fp32 (RS_F32: rounded to bf16 first); u, theta
+ * fp32 [B,H,n]; W_re, W_im fp32 [B,H,n,n] row-major (entry (i, j) of head (b, h) at
+ * ((b*H + h)*n + i)*n + j), every entry written: 0 above the diagonal and wherever G is
+ * exactly 0. The logits come from the tensor cores (bf16 inputs, fp32 accumulation); the
+ * rest is fp32. Caller-owned device memory, 16-byte aligned; workspace of at least
+ * resolvent_operator_workspace_bytes. Supported: 1 <= d <= 128 with d % 8 == 0.
+ * Errors as for resolvent_head_forward; refusals through the status word.
+ */
+rs_status resolvent_operator(const void *q, const void *k, const float *u, const float *theta,
+                             rs_switches sw, int B, int H, int n, int d, rs_dtype dtype,
+                             float *W_re, float *W_im, void *workspace, size_t workspace_bytes,
+                             int32_t *status_dev, void *stream);
+
 /* Workspace bytes resolvent_chain_scan needs for these sizes (0 when n == 0). */
 size_t resolvent_chain_workspace_bytes(int B, int H, int n, int dv);
 

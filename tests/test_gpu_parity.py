@@ -408,3 +408,53 @@ def test_chain_carry_in_alone_matches_prefixed_sequence(R):
     a1 = np.clip(u[:, 1].astype(np.float64), 0, 1) * np.exp(1j * th[:, 1].astype(np.float64))
     want1 = a1[:, None] * y[:, 0, :] + b[:, 1, :]
     assert np.max(np.abs(y[:, 1, :] - want1)) <= 1e-5 * (np.max(np.abs(want1)) + 1.0)
+
+
+# ------------------------------------------------------------------ the operator W itself
+
+OP_CASES = [
+    # B, H, n, d, dtype, beta, qk, g, u_range, zero_frac
+    (1, 1, 1, 16, "fp32", 1.0, 1.0, 0.5, (0.0, 1.0), 0.0),
+    (1, 2, 130, 64, "bf16", 1.0, 1.0, 0.5, (0.5, 1.0), 0.02),
+    (1, 2, 300, 128, "fp32", 0.5, 0.7, 0.3, (-0.5, 1.5), 0.0),
+    (1, 2, 257, 64, "bf16", 0.0, 0.0, 1.0, (0.0, 1.0), 0.05),
+    (2, 1, 200, 32, "bf16", 1.0, 1.0, 0.0, (0.0, 1.0), 0.0),
+    (1, 1, 640, 64, "bf16", 1.0, 1.0, 1.0, (0.95, 1.0), 0.004),
+]
+
+
+@pytest.mark.parametrize("case", OP_CASES, ids=[str(i) for i in range(len(OP_CASES))])
+def test_operator_matches_oracle(R, oracle_mod, case):
+    """W from resolvent_operator against the oracle's dense W, every entry: within 1e-3 of
+    the head's largest |W|, and every exact zero of the oracle (a closed gate on the path,
+    or above the diagonal) an exact zero on the GPU."""
+    B, H, n, d, dt, beta, qk, g, ur, zf = case
+    hi = W.head_inputs(B, H, n, d, 8, seed=500 + n + d, dtype=dt, q_scale=1 / math.sqrt(d),
+                       u_range=ur, zero_frac=zf, beta=beta, qk=qk, g=g)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    shp = (B, H, n)
+    Wre, Wim = R.operator(dev(hi.q.reshape(*shp, d), tdt), dev(hi.k.reshape(*shp, d), tdt),
+                          dev(hi.u.reshape(shp)), dev(hi.theta.reshape(shp)), beta, qk, g)
+    torch.cuda.synchronize()
+    Wg = (Wre.cpu().double().numpy() + 1j * Wim.cpu().double().numpy()).reshape(B * H, n, n)
+    for h in range(B * H):
+        ref = oracle_mod.operator(hi.q[h], hi.k[h], hi.u[h], hi.theta[h], f32([beta])[0],
+                                  f32([qk])[0], f32([g])[0])
+        scale = np.max(np.abs(ref))
+        assert np.max(np.abs(Wg[h] - ref)) <= 1e-3 * scale, f"{case} head {h}"
+        assert np.all(Wg[h][ref == 0] == 0), f"{case} head {h}: zero pattern"
+        assert np.all(np.triu(Wg[h], 1) == 0)
+
+
+def test_operator_rows_are_stochastic(R):
+    """beta = 1, real gates (theta = 0): every row of W sums to 1."""
+    B, H, n, d = 1, 2, 520, 64
+    hi = W.head_inputs(B, H, n, d, 8, seed=61, q_scale=1 / math.sqrt(d), u_range=(0.6, 1.0),
+                       zero_frac=0.01, theta_range=(0.0, 0.0), beta=1.0, qk=1.0, g=1.0)
+    shp = (B, H, n)
+    Wre, Wim = R.operator(dev(hi.q.reshape(*shp, d), torch.bfloat16),
+                          dev(hi.k.reshape(*shp, d), torch.bfloat16),
+                          dev(hi.u.reshape(shp)), dev(hi.theta.reshape(shp)), 1.0, 1.0, 1.0)
+    rows = Wre.double().sum(dim=-1).cpu().numpy()
+    assert np.max(np.abs(rows - 1.0)) <= 1e-4
+    assert torch.all(Wim == 0)

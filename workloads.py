@@ -234,10 +234,19 @@ def chain(B=2, H=16, n=65536, dv=64) -> ChainInputs:
                        f"chain B{B} H{H} n{n} dv{dv}")
 
 
+def operator_heads(B=1, H=8, n=4096) -> HeadInputs:
+    """Materialised operator W of gated softmax heads (the gated-softmax inputs at n = 4096):
+    B=1 H=8 n=4096 d=64 bf16; q = N(0,1)/8; u ~ U(0.9,1); theta ~ U(-0.1,0.1); (1,1,0.5)."""
+    return head_inputs(B, H, n, 64, 8, seed=SEED_BASE + 5, q_scale=1.0 / 8.0,
+                       u_range=(0.9, 1.0), theta_range=(-0.1, 0.1), beta=1.0, qk=1.0, g=0.5,
+                       name=f"operator B{B} H{H} n{n} d64")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "gated_softmax": gated_softmax,
     "long_softmax": long_softmax,
     "chain": chain,
     "mixed": mixed,
+    "operator": operator_heads,
 }
