@@ -109,14 +109,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // 128-byte swizzle, rows past `rows` read as zeros.
 // [heads, rows, cols] row-major, 128-byte swizzled boxes of 128 rows x 128 bytes:
 // bf16 inputs (box 64 x 128) or fp32 outputs (box 32 x 128).
-bool make_tmap(CUtensorMap *m, const void *base, int cols, int rows, int heads, bool f32 = false)
+bool make_tmap(CUtensorMap *m, const void *base, int cols, int rows, int heads, bool f32 = false,
+               unsigned box_rows = 128)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)cols * es, (cuuint64_t)rows * cols * es};
-    cuuint32_t box[3] = {f32 ? 32u : 64u, 128, 1};
+    cuuint32_t box[3] = {f32 ? 32u : 64u, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -372,10 +373,38 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
     return RS_OK;
 }
 
+// Workspace of resolvent_operator.
+struct OperatorWs {
+    size_t gate, prefix, suffix, carry, qpad, kpad, part, ctab, rowf, rowq, total;
+    bool copy_qk;
+};
+
+OperatorWs operator_ws(int B, int H, int n, int d, rs_dtype dt)
+{
+    OperatorWs w{};
+    const size_t BH = (size_t)B * H, tok = BH * n, nb = (size_t)(n + kBlock - 1) / kBlock;
+    const size_t slots = std::min<size_t>(BH, kMaxSlots);
+    const size_t nch = (nb + operator_chunk(n) - 1) / operator_chunk(n);
+    w.copy_qk = dt == RS_F32 || d != pad64(d);
+    size_t off = 0;
+    w.gate = off; off += up256(tok * 8);
+    w.prefix = off; off += up256(tok * 8);
+    w.suffix = off; off += up256(tok * 8);
+    w.carry = off; off += up256(BH * nb * 8);
+    w.qpad = off; off += w.copy_qk ? up256(tok * pad64(d) * 2) : 0;
+    w.kpad = off; off += w.copy_qk ? up256(tok * pad64(d) * 2) : 0;
+    w.part = off; off += up256(slots * nb * nch * 128 * 8);
+    w.ctab = off; off += up256(slots * nb * nb * 8);
+    w.rowf = off; off += up256(slots * nb * 128 * 16);
+    w.rowq = off; off += up256(slots * nb * 128 * 4);
+    w.total = off;
+    return w;
+}
+
 size_t resolvent_operator_workspace_bytes(int B, int H, int n, int d, rs_dtype dtype)
 {
     if (B <= 0 || H <= 0 || n <= 0 || d <= 0) return 0;
-    return head_ws(B, H, n, d, 64, dtype).total;
+    return operator_ws(B, H, n, d, dtype).total;
 }
 
 rs_status resolvent_operator(const void *q, const void *k, const float *u, const float *theta,
@@ -395,7 +424,7 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
     for (const void *p : {q, k, (const void *)u, (const void *)theta, (const void *)W_re,
                           (const void *)W_im, (const void *)workspace})
         if (!aligned16(p)) return RS_ERR_ALIGN;
-    const HeadWs w = head_ws(B, H, n, d, 64, dtype);
+    const OperatorWs w = operator_ws(B, H, n, d, dtype);
     if (!workspace || workspace_bytes < w.total) return RS_ERR_WORKSPACE;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -420,9 +449,14 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
         qs = qp;
         ks = kp;
     }
-    HeadMaps maps;
+    OpMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (!make_tmap(&maps.q, qs, DP, n, BH) || !make_tmap(&maps.k, ks, DP, n, BH)) return RS_ERR_CUDA;
+    // W goes out by tensor-map stores when its rows are a multiple of 16 bytes
+    const bool tma_out = n % 4 == 0;
+    if (tma_out && (!make_tmap(&maps.wre, W_re, n, n, BH, true, 32) ||
+                    !make_tmap(&maps.wim, W_im, n, n, BH, true, 32)))
+        return RS_ERR_CUDA;
     for (const HeadTable &t : tabs) {
         if (t.g[0] == 0.f) continue;  // G = 1: no gate products
         GatePrepArgs ga{};
@@ -431,15 +465,22 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
         if (launch_gate_prep(ga, t, s) != cudaSuccess) return RS_ERR_CUDA;
         ++g_launches;
     }
-    prof_mark(s, 0);
     for (const HeadTable &t : tabs) {
-        HeadArgs ha{};
-        ha.n = n; ha.d = d; ha.dv = 64; ha.gate = gate; ha.prefix = prefix; ha.suffix = suffix;
-        ha.carry = carry; ha.status = status_dev;
-        if (launch_operator(ha, t, maps, DP, W_re, W_im, s) != cudaSuccess) return RS_ERR_CUDA;
-        ++g_launches;
+        OpArgs oa{};
+        oa.n = n; oa.d = d; oa.chunk = operator_chunk(n);
+        oa.gate = gate; oa.prefix = prefix; oa.suffix = suffix; oa.carry = carry;
+        oa.W_re = W_re; oa.W_im = W_im;
+        oa.part = reinterpret_cast<float2 *>(ws + w.part);
+        oa.ctab = reinterpret_cast<float2 *>(ws + w.ctab);
+        oa.rowf = reinterpret_cast<float4 *>(ws + w.rowf);
+        oa.rowq = reinterpret_cast<float *>(ws + w.rowq);
+        oa.status = status_dev; oa.tma_out = tma_out ? 1 : 0;
+        if (launch_operator_stats(oa, t, maps, DP, s) != cudaSuccess) return RS_ERR_CUDA;
+        prof_mark(s, 0);
+        if (launch_operator(oa, t, maps, DP, s) != cudaSuccess) return RS_ERR_CUDA;
+        prof_mark(s, 1);
+        g_launches += 3;
     }
-    prof_mark(s, 1);
     return RS_OK;
 }
 

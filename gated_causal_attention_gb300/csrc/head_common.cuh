@@ -42,9 +42,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 // The same, with one answer for the whole warp (the warp then stays converged for the
 // warp-wide tcgen05.ld / tcgen05.st that follow).
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                              int32_t *status)
+                                              int32_t *status, uint32_t sleep_ns = 32)
 {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status, 32));
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status, sleep_ns));
 }
 
 __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32])

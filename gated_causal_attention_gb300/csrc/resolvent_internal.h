@@ -99,9 +99,31 @@ struct HeadMaps {
 // dpad, dvpad in {64, 128}
 cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps,
                             int dpad, int dvpad, cudaStream_t s);
-// The materialised operator W [n, n] (operator.cu): one launch per table of heads of one kind.
-cudaError_t launch_operator(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps, int dpad,
-                            float *W_re, float *W_im, cudaStream_t s);
+
+// ---------------------------------------------------------------- materialised operator (K4)
+struct OpArgs {
+    int n, d;
+    int chunk;                   // key tiles per row-statistics unit (operator_chunk(n))
+    const float2 *gate, *prefix, *suffix, *carry;  // gate products of K1 (gated heads)
+    float *W_re, *W_im;          // [BH, n, n]
+    float2 *part;                // [slots, nqt, ceil(nqt / chunk), 128] partial (M, Z) per row
+    float2 *ctab;                // [slots, nqt, nqt] carry products C(QB, KB)
+    float4 *rowf;                // [slots, nqt * 128] (M, f, f prefix_i) per row
+    float *rowq;                 // [slots, nqt * 128] |prefix_i| (1 ungated; 0 past n)
+    int32_t *status;
+    int tma_out;                 // W written by tensor-map stores (n % 4 == 0); else plain stores
+};
+// q, k (bf16, box 64 x 128) and, when tma_out is set, W_re and W_im (fp32, box 32 x 32).
+struct OpMaps {
+    CUtensorMap q, k, wre, wim;
+};
+int operator_chunk(int n);
+// Row statistics (partials and carry products, then the merged row data: two launches),
+// then W; per table of heads of one kind, in this order on one stream.
+cudaError_t launch_operator_stats(const OpArgs &a, const HeadTable &tab, const OpMaps &maps, int dpad,
+                                  cudaStream_t s);
+cudaError_t launch_operator(const OpArgs &a, const HeadTable &tab, const OpMaps &maps, int dpad,
+                            cudaStream_t s);
 
 // ---------------------------------------------------------------- debug path product
 cudaError_t launch_debug_path_product(const float2 *gate, const float2 *prefix,
