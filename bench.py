@@ -183,9 +183,9 @@ class Clocks:
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
-KERNEL_SOURCES = {"head_fwd_kernel": ["head_fwd.cu", "common.cuh", "gate_products.cuh"],
+KERNEL_SOURCES = {"head_fwd_kernel": ["head_fwd.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"],
                   "chain_scan_kernel": ["chain_scan.cu", "common.cuh"],
-                  "operator_kernel": ["operator.cu", "common.cuh", "gate_products.cuh"]}
+                  "operator_kernel": ["operator.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"]}
 
 
 def measured_traffic(kernel, workload):
