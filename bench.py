@@ -499,7 +499,7 @@ def run_ours(args):
                "sample": (f"{toks // inp.n} whole heads" if is_chain else
                           f"{toks // (inp.n * inp.n)} whole heads' W" if is_op else
                           f"{toks // (inp.B * inp.H)} seeded random rows of each of the "
-                          f"{inp.B * inp.H} heads") + f" ({toks} tokens, {secs:.1f} s)"}
+                          f"{inp.B * inp.H} heads") + f" ({toks} {'entries' if is_op else 'tokens'}, {secs:.1f} s)"}
 
     if rank == 0:
         line = {"metric": ("chain tokens/s (B*H*n/s)" if is_chain else
