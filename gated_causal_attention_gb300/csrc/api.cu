@@ -107,8 +107,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // 3-D view [heads, rows, cols] of a bf16 tensor; boxes of 64 columns x 128 rows x 1 head,
 // 128-byte swizzle, rows past `rows` read as zeros.
-// [heads, rows, cols] row-major, 128-byte swizzled boxes of 128 rows x 128 bytes:
-// bf16 inputs (box 64 x 128) or fp32 outputs (box 32 x 128).
+}  // namespace
+
+int rs::device_sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+namespace {
+
+// [heads, rows, cols] row-major, 128-byte swizzled boxes of box_rows rows x 128 bytes:
+// bf16 inputs (box 64 x 128) or fp32 outputs (box 32 x box_rows).
 bool make_tmap(CUtensorMap *m, const void *base, int cols, int rows, int heads, bool f32 = false,
                unsigned box_rows = 128)
 {
@@ -127,7 +144,7 @@ bool make_tmap(CUtensorMap *m, const void *base, int cols, int rows, int heads, 
 
 // Workspace of resolvent_head_forward.
 struct HeadWs {
-    size_t gate, prefix, suffix, carry, qpad, kpad, vpad, chain, total;
+    size_t gate, prefix, suffix, carry, numkv, qpad, kpad, vpad, chain, total;
     bool copy_qk, copy_v;
 };
 
@@ -142,6 +159,7 @@ HeadWs head_ws(int B, int H, int n, int d, int dv, rs_dtype dt)
     w.prefix = off; off += up256(tok * 8);
     w.suffix = off; off += up256(tok * 8);
     w.carry = off; off += up256(BH * nb * 8);
+    w.numkv = off; off += up256(std::min<size_t>(BH, kMaxSlots) * nb * 4);
     w.qpad = off; off += w.copy_qk ? up256(tok * pad64(d) * 2) : 0;
     w.kpad = off; off += w.copy_qk ? up256(tok * pad64(d) * 2) : 0;
     w.vpad = off; off += w.copy_v ? up256(tok * pad64(dv) * 2) : 0;
@@ -342,6 +360,18 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
         if (tma_out && (!make_tmap(&maps.ore, O_re, dv, n, BH, true) ||
                         !make_tmap(&maps.oim, O_im, dv, n, BH, true)))
             return RS_ERR_CUDA;
+        std::vector<HeadArgs> args;
+        for (const HeadTable &t : head_tabs) {
+            HeadArgs ha{};
+            ha.n = n; ha.d = d; ha.dv = dv; ha.gate = gate; ha.prefix = prefix; ha.suffix = suffix;
+            ha.carry = carry; ha.O_re = O_re; ha.O_im = O_im; ha.status = status_dev;
+            ha.tma_out = tma_out ? 1 : 0;
+            ha.numkv = reinterpret_cast<int *>(ws + w.numkv);
+            // about 24 MB of K and V per head group: a group's K/V tiles stay in L2
+            const size_t kv_head = (size_t)n * (DP + DVP) * 2;
+            ha.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / kv_head));
+            args.push_back(ha);
+        }
         for (const HeadTable &t : head_tabs) {
             GatePrepArgs ga{};
             ga.u = u; ga.theta = theta; ga.n = n; ga.gate = gate; ga.prefix = prefix;
@@ -349,16 +379,15 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
             if (launch_gate_prep(ga, t, s) != cudaSuccess) return RS_ERR_CUDA;
             ++g_launches;
         }
+        // The per-tile key-tile counts share one scratch array, so each table's count runs
+        // right before its head launch (same stream).
         prof_mark(s, 0);
-        for (const HeadTable &t : head_tabs) {
-            HeadArgs ha{};
-            ha.n = n; ha.d = d; ha.dv = dv; ha.gate = gate; ha.prefix = prefix; ha.suffix = suffix;
-            ha.carry = carry; ha.O_re = O_re; ha.O_im = O_im; ha.status = status_dev;
-            ha.tma_out = tma_out ? 1 : 0;
-            // about 24 MB of K and V per head group: a group's K/V tiles stay in L2
-            const size_t kv_head = (size_t)n * (DP + DVP) * 2;
-            ha.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / kv_head));
-            if (launch_head_fwd(ha, t, maps, DP, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
+        for (size_t i = 0; i < head_tabs.size(); ++i) {
+            if (head_tabs[i].g[0] != 0.f) {
+                if (launch_head_numkv(args[i], head_tabs[i], s) != cudaSuccess) return RS_ERR_CUDA;
+                ++g_launches;
+            }
+            if (launch_head_fwd(args[i], head_tabs[i], maps, DP, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
             ++g_launches;
         }
         prof_mark(s, 1);

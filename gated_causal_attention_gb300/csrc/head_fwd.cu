@@ -11,9 +11,9 @@
 //   producer warp 0   TMA: Q once, then K and V tiles (one K+V ring for gated heads, a K
 //                     ring and a V ring for g = 0 heads);
 //   producer warp 1   issues S(t) = Q K(t)^T into one of 2-3 TMEM S buffers;
-//   producer warp 2   counts the key tiles, then issues O += P(t) V'(t) with P read from
-//                     TMEM (it overwrites S). Two issuers, because a tcgen05.mma is accepted
-//                     only about as fast as the pipe retires the previous one;
+//   producer warp 2   issues O += P(t) V'(t) with P read from TMEM (it overwrites S). Two
+//                     issuers, because a tcgen05.mma is accepted only about as fast as the
+//                     pipe retires the previous one;
 //   softmax halves    two threads per query row, keys [0,64) and [64,128) of each tile:
 //                     live-masked running maximum M (moved only when it grows by more than
 //                     2^8, so the accumulator is rarely rescaled), P = 2^{t - M} packed to
@@ -28,6 +28,8 @@
 // from the top of each half down (rows of the upper half start the lower half from
 // A_i = a_64 ... a_i), and two MMAs accumulate Re(P G) V and Im(P G) V.
 // Heads with g = 0 have G = 1: no gate products, no value preparation, a real accumulator.
+// The number of live off-diagonal key tiles of each query tile comes from a small launch
+// before (head_numkv_kernel), so the CTA starts its loads right after one barrier.
 // The epilogue stages O in the freed K/V ring and writes it with tensor-map stores.
 //
 // Every wait is bounded: one that runs out raises RS_STATUS_TIMEOUT, tells the other roles
@@ -40,8 +42,8 @@ namespace {
 
 using namespace head;
 
-// Warpgroup roles: 0 the producer (warp 0 loads by TMA, warp 1 issues S, warp 2 counts the
-// key tiles and then issues P V), 1 and 2 softmax (each query row has one thread in each:
+// Warpgroup roles: 0 the producer (warp 0 loads by TMA, warp 1 issues S, warp 2 issues
+// P V), 1 and 2 softmax (each query row has one thread in each:
 // keys 0-63 and 64-127 of every key tile), 3 value preparation (gated heads only).
 // After the prologue the producer (and value-prep) warpgroups hand registers to the softmax
 // warpgroups (setmaxnreg); the shares add up to exactly what the launch provides:
@@ -95,9 +97,10 @@ struct Cfg {
     static constexpr uint32_t upA = zpart + 128 * 4;                  // float2 [128] prod a_{64..i}
     static constexpr uint32_t upR = upA + 128 * 8;                    // float [128] prod |a_{64..i}|
     static constexpr uint32_t bars = upR + 128 * 4;                   // mbarriers
-    // q; full, empty, vprep, rc (4 each); s_full, p_full, pv_done (3 each); vfull, vempty (4 each)
-    static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4;
-    static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, numkv, abort
+    // q; full, empty, vprep, rc (4 each); s_full, p_full, pv_done (3 each); vfull, vempty
+    // (4 each); diag_ready
+    static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4 + 1;
+    static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, (unused), abort
     static constexpr uint32_t end = misc + 64;
     static constexpr uint32_t alloc = end + 1024;
     static constexpr uint32_t acc_cols = GATED ? 2 * DVP : DVP;
@@ -120,6 +123,7 @@ struct Cfg {
 struct Barriers {
     // full/empty: the K+V ring (gated heads) or the K ring (g = 0); vfull/vempty: the V ring
     uint64_t *q, *full, *empty, *vprep, *rc, *s_full, *p_full, *pv_done, *vfull, *vempty;
+    uint64_t *diag_ready;  // the value-prep warps have written the query block's gate data
 };
 
 template <int DP, int DVP, bool GATED>
@@ -135,11 +139,10 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bar0 = reinterpret_cast<uint64_t *>(smem + L::bars);
-    Barriers B{bar0,      bar0 + 1,  bar0 + 5,  bar0 + 9,  bar0 + 13,
-               bar0 + 17, bar0 + 20, bar0 + 23, bar0 + 26, bar0 + 30};
+    Barriers B{bar0,      bar0 + 1,  bar0 + 5,  bar0 + 9,  bar0 + 13, bar0 + 17,
+               bar0 + 20, bar0 + 23, bar0 + 26, bar0 + 30, bar0 + 34};
     int *misc = reinterpret_cast<int *>(smem + L::misc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
-    int *s_numkv = misc + 1;
     volatile int *s_abort = misc + 2;
     float *s_rc = reinterpret_cast<float *>(smem + L::rc);
     float2 *s_ga = reinterpret_cast<float2 *>(smem + L::ga);
@@ -174,6 +177,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             uint32_t count = 1;                                       // TMA / tcgen05.commit
             if (b >= B.vprep && b < B.vprep + 8) count = 4;           // value-prep warps (vprep, rc)
             if (b >= B.p_full && b < B.p_full + 3) count = 8;         // softmax warps, both halves
+            if (b == B.diag_ready) count = 4;                          // value-prep warps
             mbar_init(bar0 + i, count);
         }
         *s_abort = 0;
@@ -195,102 +199,14 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     const int r = tid & 127;  // query row (softmax) or key row (value prep)
     const int row = sQ + r;
     const bool valid = softmax && row < n;
-    cplx pq = {0.f, 0.f};
-    float rq = 0.f;
-    if (valid) {
-        if (GATED) {
-            const float2 v = a.prefix[tok0 + row];
-            pq = {v.x, v.y};
-            rq = cabs(pq);
-        } else {
-            pq = {1.f, 0.f};
-            rq = 1.f;
-        }
-    }
-    if (GATED && wg == RL::vprep_wg) {  // the query block's own gates, for the diagonal tile
-        float2 av = make_float2(0.f, 0.f);
-        if (sQ + r < n) av = a.gate[tok0 + sQ + r];
-        s_ga[r] = av;
-        s_gm[r] = cabs({av.x, av.y});
-        if (r < 32) {
-            // rows of the upper half of the block: A_i = a_64 a_65 ... a_i (and its modulus
-            // product), so that keys of the lower half factor as A_i * prod_{k=j+1..63} a_k.
-            // Lane l holds rows 64 + 2l and 65 + 2l; a warp scan over the pair products.
-            const int i0 = 64 + 2 * r;
-            float2 g0 = make_float2(0.f, 0.f), g1 = make_float2(0.f, 0.f);
-            if (sQ + i0 < n) g0 = a.gate[tok0 + sQ + i0];
-            if (sQ + i0 + 1 < n) g1 = a.gate[tok0 + sQ + i0 + 1];
-            const cplx c0 = {g0.x, g0.y}, c1 = {g1.x, g1.y};
-            const float m0 = cabs(c0), m1 = cabs(c1);
-            cplx incl = cmul(c0, c1);
-            float rincl = m0 * m1;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const cplx y = shfl_up(incl, d);
-                const float ry = __shfl_up_sync(0xffffffffu, rincl, d);
-                if (r >= d) {
-                    incl = cmul(y, incl);
-                    rincl = ry * rincl;
-                }
-            }
-            cplx excl = shfl_up(incl, 1);
-            float rexcl = __shfl_up_sync(0xffffffffu, rincl, 1);
-            if (r == 0) {
-                excl = {1.f, 0.f};
-                rexcl = 1.f;
-            }
-            const cplx A0 = cmul(excl, c0);
-            s_upA[i0] = make_float2(A0.re, A0.im);
-            s_upA[i0 + 1] = make_float2(incl.re, incl.im);
-            s_upR[i0] = rexcl * m0;
-            s_upR[i0 + 1] = rincl;
-        }
-    }
-    // the key-tile counter's first 32 block totals, loaded before the barrier
-    float2 carry0 = make_float2(1.f, 0.f);
-    if (GATED && warp == kPvWarp && lane < QB) carry0 = a.carry[(int64_t)bh * nqt + QB - 1 - lane];
+    // off-diagonal key tiles: up to the first exactly-zero carry (gated heads, counted by
+    // head_numkv_kernel), every earlier tile otherwise
+    const int numkv = GATED ? a.numkv[slot * nqt + QB] : QB;
+    const int T = numkv + 1;  // tiles: numkv off-diagonal, then the diagonal
     tc_fence_before();
-    const int rows_alive = __syncthreads_or(valid && rq > 0.f);
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    // number of off-diagonal key tiles: stop at the first tile whose carry C is exactly 0
-    if (warp == kPvWarp) {
-        int numkv = rows_alive ? QB : 0;
-        if (GATED && numkv > 0) {
-            const float2 *T = a.carry + (int64_t)bh * nqt;
-            cplx run = {1.f, 0.f};
-            for (int base = 0; base < QB; base += 32) {
-                const int t = base + lane;
-                cplx x = {1.f, 0.f};
-                if (base == 0) {
-                    x = {carry0.x, carry0.y};
-                } else if (t < QB) {
-                    const float2 v = T[QB - 1 - t];
-                    x = {v.x, v.y};
-                }
-                cplx incl = x;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const cplx y = shfl_up(incl, d);
-                    if (lane >= d) incl = cmul(y, incl);
-                }
-                cplx excl = shfl_up(incl, 1);
-                if (lane == 0) excl = {1.f, 0.f};
-                const cplx Ct = cmul(run, excl);  // carry of tile t
-                const unsigned z = __ballot_sync(0xffffffffu, t < QB && !cnonzero(Ct));
-                if (z) {
-                    numkv = base + __ffs(z) - 1;
-                    break;
-                }
-                run = cmul(run, shfl_idx(incl, 31));
-            }
-        }
-        if (lane == 0) *s_numkv = numkv;
-    }
-    __syncthreads();
-    const int numkv = *s_numkv;
-    const int T = numkv + 1;  // tiles: numkv off-diagonal, then the diagonal
 
     // Registers move from the producer (and value-prep) warps to the softmax warps: each role
     // starts with its setmaxnreg; the shares add up to exactly what the CTA was launched with.
@@ -466,9 +382,66 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             if (lane == 0) mbar_arrive(B.vprep + st);
             C = carry_step(C, {Tv.x, Tv.y});
         }
+        // the query block's own gates, for the diagonal tile (read by the softmax rows once
+        // diag_ready completes)
+        {
+            float2 av = make_float2(0.f, 0.f);
+            if (sQ + r < n) av = a.gate[tok0 + sQ + r];
+            s_ga[r] = av;
+            s_gm[r] = cabs({av.x, av.y});
+            if (r < 32) {
+                // rows of the upper half of the block: A_i = a_64 a_65 ... a_i (and its modulus
+                // product), so that keys of the lower half factor as A_i * prod_{k=j+1..63} a_k.
+                // Lane l holds rows 64 + 2l and 65 + 2l; a warp scan over the pair products.
+                const int i0 = 64 + 2 * r;
+                float2 g0 = make_float2(0.f, 0.f), g1 = make_float2(0.f, 0.f);
+                if (sQ + i0 < n) g0 = a.gate[tok0 + sQ + i0];
+                if (sQ + i0 + 1 < n) g1 = a.gate[tok0 + sQ + i0 + 1];
+                const cplx c0 = {g0.x, g0.y}, c1 = {g1.x, g1.y};
+                const float m0 = cabs(c0), m1 = cabs(c1);
+                cplx incl = cmul(c0, c1);
+                float rincl = m0 * m1;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const cplx y = shfl_up(incl, d);
+                    const float ry = __shfl_up_sync(0xffffffffu, rincl, d);
+                    if (r >= d) {
+                        incl = cmul(y, incl);
+                        rincl = ry * rincl;
+                    }
+                }
+                cplx excl = shfl_up(incl, 1);
+                float rexcl = __shfl_up_sync(0xffffffffu, rincl, 1);
+                if (r == 0) {
+                    excl = {1.f, 0.f};
+                    rexcl = 1.f;
+                }
+                const cplx A0 = cmul(excl, c0);
+                s_upA[i0] = make_float2(A0.re, A0.im);
+                s_upA[i0 + 1] = make_float2(incl.re, incl.im);
+                s_upR[i0] = rexcl * m0;
+                s_upR[i0 + 1] = rincl;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.diag_ready);
+        }
     } else if (softmax) {
         // ------------------------------------------------------------ softmax rows
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RL::softmax_regs));
+        // the row factor prefix_i (loaded after the CTA's barrier: it is first needed with the
+        // first tile's logits)
+        cplx pq = {0.f, 0.f};
+        float rq = 0.f;
+        if (valid) {
+            if (GATED) {
+                const float2 v = a.prefix[tok0 + row];
+                pq = {v.x, v.y};
+                rq = cabs(pq);
+            } else {
+                pq = {1.f, 0.f};
+                rq = 1.f;
+            }
+        }
         // Two threads per query row: half h takes keys [64h, 64h + 64) of every key tile.
         const int h = wg - RL::sm_wg0;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -628,6 +601,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             const int jstop = i < jtop ? i : jtop;  // a_{j+1} enters the product for j < jstop
             const bool from_upper = GATED && h == 0 && i > 63;
             bool ready = ok && wait_bar_warp(B.s_full + sb, (t / L::NSB) & 1, s_abort, a.status);
+            if (GATED && ready) ready = wait_bar_warp(B.diag_ready, 0, s_abort, a.status);
             tc_fence_after();
             uint32_t s[64];
             if (ready) {
@@ -825,6 +799,47 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     }
 }
 
+// Off-diagonal key tiles of each query tile of a table of gated heads: the key tiles run from
+// KB = QB - 1 down and stop at the first one whose carry C(QB, KB) is exactly 0 (every
+// farther tile is then exactly dead). One warp per query tile; the carries are scanned 32
+// block totals at a time.
+__global__ void __launch_bounds__(128)
+head_numkv_kernel(HeadArgs a, const __grid_constant__ HeadTable tab)
+{
+    const int lane = threadIdx.x & 31;
+    const int nqt = (a.n + 127) / 128;
+    const int item = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (item >= nqt * tab.count) return;
+    const int slot = item / nqt, QB = item - slot * nqt;
+    const float2 *T = a.carry + (int64_t)tab.bh[slot] * nqt;
+    int numkv = QB;
+    cplx run = {1.f, 0.f};
+    for (int base = 0; base < QB; base += 32) {
+        const int t = base + lane;
+        cplx x = {1.f, 0.f};
+        if (t < QB) {
+            const float2 v = T[QB - 1 - t];
+            x = {v.x, v.y};
+        }
+        cplx incl = x;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const cplx y = shfl_up(incl, d);
+            if (lane >= d) incl = cmul(y, incl);
+        }
+        cplx excl = shfl_up(incl, 1);
+        if (lane == 0) excl = {1.f, 0.f};
+        const cplx Ct = cmul(run, excl);  // carry of tile t
+        const unsigned z = __ballot_sync(0xffffffffu, t < QB && !cnonzero(Ct));
+        if (z) {
+            numkv = base + __ffs(z) - 1;
+            break;
+        }
+        run = cmul(run, shfl_idx(incl, 31));
+    }
+    if (lane == 0) a.numkv[slot * nqt + QB] = numkv;
+}
+
 template <int DP, int DVP, bool GATED>
 cudaError_t launch_t(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps, cudaStream_t s)
 {
@@ -862,6 +877,14 @@ cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const HeadM
     // one launch serves heads of one kind: the caller splits gated and ungated heads
     return tab.g[0] != 0.f ? launch_g<true>(a, tab, maps, dpad, dvpad, s)
                            : launch_g<false>(a, tab, maps, dpad, dvpad, s);
+}
+
+cudaError_t launch_head_numkv(const HeadArgs &a, const HeadTable &tab, cudaStream_t s)
+{
+    if (tab.count == 0 || a.n == 0) return cudaSuccess;
+    const int tiles = (a.n + 127) / 128 * tab.count;
+    head_numkv_kernel<<<(tiles + 3) / 4, 128, 0, s>>>(a, tab);
+    return cudaGetLastError();
 }
 
 }  // namespace rs

@@ -735,19 +735,6 @@ operator_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __grid_co
     op_teardown(tmem);
 }
 
-int sm_count()
-{
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-        cached[dev] = v;
-    }
-    return cached[dev];
-}
-
 template <int DP, bool GATED>
 cudaError_t launch_stats(const OpArgs &a, const HeadTable &tab, const OpMaps &maps, cudaStream_t s)
 {
@@ -759,7 +746,7 @@ cudaError_t launch_stats(const OpArgs &a, const HeadTable &tab, const OpMaps &ma
     int per_head = 0;
     for (int c = 0; c < NCH; ++c) per_head += nqt - c * a.chunk;
     const int units = per_head * tab.count;
-    const int grid = std::max(1, std::min(units, 2 * sm_count()));
+    const int grid = std::max(1, std::min(units, 2 * device_sm_count()));
     k<<<grid, kOpThreads, L::alloc, s>>>(a, tab, maps);
     return cudaGetLastError();
 }
@@ -781,7 +768,7 @@ cudaError_t launch_write(const OpArgs &a, const HeadTable &tab, const OpMaps &ma
     if (e != cudaSuccess) return e;
     const int nqt = (a.n + 127) / 128;
     const int64_t tiles = (int64_t)nqt * nqt * tab.count;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count()));
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
     k<<<grid, kOpThreads, L::alloc, s>>>(a, tab, maps);
     return cudaGetLastError();
 }

@@ -90,12 +90,16 @@ struct HeadArgs {
     int32_t *status;
     int tma_out;  // O_re / O_im written by tensor-map stores (dv % 4 == 0); else plain stores
     int heads_per_group;  // blocks are ordered head group by head group (1 <= it <= table count)
+    int *numkv;           // [slots * nqt] off-diagonal key tiles of each query tile (gated heads)
 };
 // The tensor maps of one head launch: q, k, v (bf16, box 64 x 128) and, when tma_out is set,
 // O_re and O_im (fp32, box 32 x 128).
 struct HeadMaps {
     CUtensorMap q, k, v, ore, oim;
 };
+// The number of off-diagonal key tiles of every query tile of a table of gated heads, into
+// a.numkv (one warp per tile; launched right before that table's head launch).
+cudaError_t launch_head_numkv(const HeadArgs &a, const HeadTable &tab, cudaStream_t s);
 // dpad, dvpad in {64, 128}
 cudaError_t launch_head_fwd(const HeadArgs &a, const HeadTable &tab, const HeadMaps &maps,
                             int dpad, int dvpad, cudaStream_t s);
@@ -118,6 +122,8 @@ struct OpMaps {
     CUtensorMap q, k, wre, wim;
 };
 int operator_chunk(int n);
+// Multiprocessors of the current device (looked up once per device).
+int device_sm_count();
 // Row statistics (partials and carry products, then the merged row data: two launches),
 // then W; per table of heads of one kind, in this order on one stream.
 cudaError_t launch_operator_stats(const OpArgs &a, const HeadTable &tab, const OpMaps &maps, int dpad,
