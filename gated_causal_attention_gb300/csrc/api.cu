@@ -355,11 +355,8 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
         if (!make_tmap(&maps.q, qs, DP, n, BH) || !make_tmap(&maps.k, ks, DP, n, BH) ||
             !make_tmap(&maps.v, vs, DVP, n, BH))
             return RS_ERR_CUDA;
-        // the outputs go out by tensor-map stores when their rows are a multiple of 16 bytes
+        // the outputs leave by 16-byte stores when their rows are a multiple of 16 bytes
         const bool tma_out = dv % 4 == 0;
-        if (tma_out && (!make_tmap(&maps.ore, O_re, dv, n, BH, true) ||
-                        !make_tmap(&maps.oim, O_im, dv, n, BH, true)))
-            return RS_ERR_CUDA;
         std::vector<HeadArgs> args;
         for (const HeadTable &t : head_tabs) {
             HeadArgs ha{};

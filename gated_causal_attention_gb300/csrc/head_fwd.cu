@@ -30,7 +30,7 @@
 // Heads with g = 0 have G = 1: no gate products, no value preparation, a real accumulator.
 // The number of live off-diagonal key tiles of each query tile comes from a small launch
 // before (head_numkv_kernel), so the CTA starts its loads right after one barrier.
-// The epilogue stages O in the freed K/V ring and writes it with tensor-map stores.
+// The epilogue stages O in the freed K/V ring and writes it with coalesced 16-byte stores.
 //
 // Every wait is bounded: one that runs out raises RS_STATUS_TIMEOUT, tells the other roles
 // to stop, and the CTA winds down with its TMEM freed.
@@ -722,8 +722,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             if (done) {
                 tc_fence_after();
                 if (a.tma_out) {
-                    // stage 128 rows x 32 columns per chunk in the free K/V ring, 128-byte
-                    // swizzled as the tensor map expects, then store it with one bulk copy
+                    // stage 128 rows x 32 columns per chunk in the free K/V ring, 16-byte units
+                    // rotated by the row (r & 7) so that the row-wise writes here and the
+                    // row-segment reads below both spread over all banks
                     const uint32_t stage_re = sbase + L::stages;
                     const uint32_t stage_im = stage_re + nq * kRegion;
 #pragma unroll 1
@@ -749,24 +750,36 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                             if (GATED) sts128(stage_im + off, make_uint4(wi[0], wi[1], wi[2], wi[3]));
                         }
                     }
-                    if (!GATED) {  // Im O = 0: one zero chunk, stored nq times
-                        const uint32_t z = stage_im + (uint32_t)(h * 128 + r) * 64;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) sts128(z + c * 16, make_uint4(0u, 0u, 0u, 0u));
-                    }
-                    fence_proxy_async_smem();
                 }
             }
             done = named_bar_and(kBarSoftmax, 256, done);
-            if (done && a.tma_out && h == 0 && r == 0) {
+            if (done && a.tma_out) {
+                // The staged chunks leave with coalesced 16-byte stores: lane l of each warp takes
+                // 16-byte unit l % 8 of row l / 8 of a group of four rows, so one instruction
+                // writes four whole 128-byte row segments. No copy engine is involved, so the CTA
+                // need not wait for anything before it ends.
                 const uint32_t stage_re = sbase + L::stages;
                 const uint32_t stage_im = stage_re + nq * kRegion;
+                const int wi = (tid - RL::sm_wg0 * 128) >> 5;  // 0..7 over both halves
+                const int unit = lane & 7;
+                const int nrows = min(128, n - sQ);
+#pragma unroll 1
                 for (int q = 0; q < nq; ++q) {
-                    tma_store_3d(&maps.ore, stage_re + q * kRegion, 32 * q, sQ, bh);
-                    tma_store_3d(&maps.oim, GATED ? stage_im + q * kRegion : stage_im, 32 * q, sQ, bh);
+                    const int col = 32 * q + 4 * unit;
+                    if (col >= a.dv) continue;  // dv % 4 == 0: whole 16-byte units
+                    float *ore = a.O_re + (tok0 + sQ) * (int64_t)a.dv + col;
+                    float *oim = a.O_im + (tok0 + sQ) * (int64_t)a.dv + col;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int rr = 32 * k + 4 * wi + (lane >> 3);  // rows 0..127 over the 8 warps
+                        if (rr >= nrows) continue;
+                        const uint32_t off = q * kRegion + rr * 128 + ((unit ^ (rr & 7)) << 4);
+                        const uint4 vr = lds128(stage_re + off);
+                        *reinterpret_cast<uint4 *>(ore + (int64_t)rr * a.dv) = vr;
+                        const uint4 vi = GATED ? lds128(stage_im + off) : make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(oim + (int64_t)rr * a.dv) = vi;
+                    }
                 }
-                bulk_commit_group();
-                bulk_wait_read_all();  // the staging area must outlive the reads of the stores
             }
             if (done && !a.tma_out) {  // rows of dv % 4 != 0 floats: plain stores
                 float *ore = a.O_re + (tok0 + row) * (int64_t)a.dv;

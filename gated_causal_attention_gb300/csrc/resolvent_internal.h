@@ -88,14 +88,13 @@ struct HeadArgs {
     const float2 *gate, *prefix, *suffix, *carry;  // gate products of K1 (gated heads)
     float *O_re, *O_im;
     int32_t *status;
-    int tma_out;  // O_re / O_im written by tensor-map stores (dv % 4 == 0); else plain stores
+    int tma_out;  // O staged in shared memory and written by coalesced 16-byte stores (dv % 4 == 0); else plain stores
     int heads_per_group;  // blocks are ordered head group by head group (1 <= it <= table count)
     int *numkv;           // [slots * nqt] off-diagonal key tiles of each query tile (gated heads)
 };
-// The tensor maps of one head launch: q, k, v (bf16, box 64 x 128) and, when tma_out is set,
-// O_re and O_im (fp32, box 32 x 128).
+// The tensor maps of one head launch: q, k, v (bf16, box 64 x 128).
 struct HeadMaps {
-    CUtensorMap q, k, v, ore, oim;
+    CUtensorMap q, k, v;
 };
 // The number of off-diagonal key tiles of every query tile of a table of gated heads, into
 // a.numkv (one warp per tile; launched right before that table's head launch).
