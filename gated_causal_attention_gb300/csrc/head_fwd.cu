@@ -100,7 +100,7 @@ struct Cfg {
     // q; full, empty, vprep, rc (4 each); s_full, p_full, pv_done (3 each); vfull, vempty
     // (4 each); diag_ready
     static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4 + 1;
-    static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, (unused), abort
+    static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, -, abort, -, diag_all_live[4]
     static constexpr uint32_t end = misc + 64;
     static constexpr uint32_t alloc = end + 1024;
     static constexpr uint32_t acc_cols = GATED ? 2 * DVP : DVP;
@@ -144,6 +144,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     int *misc = reinterpret_cast<int *>(smem + L::misc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 2;
+    int *s_diaglive = misc + 4;  // [4] per value-prep warp: its gates all have modulus >= 1/2
     float *s_rc = reinterpret_cast<float *>(smem + L::rc);
     float2 *s_ga = reinterpret_cast<float2 *>(smem + L::ga);
     float *s_gm = reinterpret_cast<float *>(smem + L::gm);
@@ -388,7 +389,13 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             float2 av = make_float2(0.f, 0.f);
             if (sQ + r < n) av = a.gate[tok0 + sQ + r];
             s_ga[r] = av;
-            s_gm[r] = cabs({av.x, av.y});
+            const float am = cabs({av.x, av.y});
+            s_gm[r] = am;
+            // with every |a_k| >= 1/2, a product of at most 127 of them is at least 2^-127 > 0:
+            // no diagonal-block entry j <= i is dead, and the softmax rows skip the live test
+            // (one flag per value-prep warp)
+            const bool big = __all_sync(0xffffffffu, am >= 0.5f || sQ + r >= n);
+            if (lane == 0) s_diaglive[warp & 3] = big;
             if (r < 32) {
                 // rows of the upper half of the block: A_i = a_64 a_65 ... a_i (and its modulus
                 // product), so that keys of the lower half factor as A_i * prod_{k=j+1..63} a_k.
@@ -610,8 +617,37 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 tmem_ld_wait();
             }
             // pass 1: live maximum over j <= i
+            const bool all_live = !GATED || (s_diaglive[0] && s_diaglive[1] && s_diaglive[2] && s_diaglive[3]);
             float mt = -INFINITY;
-            if (ready) {
+            if (ready && all_live) {
+                // every entry j <= i is live: a causal extremum of the raw logits (max, or min
+                // for qk < 0), scaled once
+                float hx[4];
+                if (scale2 >= 0.f) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hx[e] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        const int j = 64 * h + e;
+                        const float v0 = j <= i ? __uint_as_float(s[e]) : -INFINITY;
+                        const float v1 = j + 1 <= i ? __uint_as_float(s[e + 1]) : -INFINITY;
+                        hx[(e >> 1) & 3] = max3f(hx[(e >> 1) & 3], v0, v1);
+                    }
+                    mt = max3f(hx[0], hx[1], fmaxf(hx[2], hx[3])) * scale2;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hx[e] = INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        const int j = 64 * h + e;
+                        const float v0 = j <= i ? __uint_as_float(s[e]) : INFINITY;
+                        const float v1 = j + 1 <= i ? __uint_as_float(s[e + 1]) : INFINITY;
+                        hx[(e >> 1) & 3] = min3f(hx[(e >> 1) & 3], v0, v1);
+                    }
+                    mt = min3f(hx[0], hx[1], fminf(hx[2], hx[3])) * scale2;
+                }
+                if (!valid || i < 64 * h) mt = -INFINITY;
+            } else if (ready) {
                 float R = from_upper ? s_upR[i] : 1.f;
 #pragma unroll
                 for (int e = 63; e >= 0; --e) {
@@ -660,7 +696,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                         const bool causal = valid && j <= i;
                         const float x = fmaf(__uint_as_float(s[32 * c + e]), scale2, -M2);
                         if (causal) chk = fmaf(x, 0.f, chk);
-                        const bool live = causal && R > 0.f;
+                        const bool live = causal && (all_live || R > 0.f);
                         const float p = live ? ex2_approx(x) : 0.f;
                         Zs = GATED ? fmaf(R, p, Zs) : Zs + p;
                         const float pr = GATED ? G.re * p : p;
