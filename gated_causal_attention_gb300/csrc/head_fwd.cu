@@ -63,7 +63,9 @@ struct Roles {
                       threads * launch_regs,
                   "register shares exceed the launch");
 };
-constexpr int kBarSoftmax = 1, kBarVprep = 2;
+// Named barriers: all softmax threads; the value-prep warps; and, per lane quarter q, the two
+// softmax warps (one per half) that hold rows 32q..32q+31.
+constexpr int kBarSoftmax = 1, kBarVprep = 2, kBarRows0 = 3;
 
 template <int DP, int DVP, bool GATED>
 struct Cfg {
@@ -529,7 +531,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             // this tile happen before either half writes P over it, and lets both halves
             // leave together if a wait ran out
             s_hmax[((t & 1) * 2 + h) * 128 + r] = mt;
-            ok = named_bar_and(kBarSoftmax, 256, ready && !*s_abort);
+            ok = named_bar_and(kBarRows0 + (warp & 3), 64, ready && !*s_abort);
             if (!ok) break;
             mt = fmaxf(mt, s_hmax[((t & 1) * 2 + (h ^ 1)) * 128 + r]);
             // move the maximum only when it grows by more than 2^8 (or is first set)
@@ -663,7 +665,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             }
             // the exchange also orders every S read of this tile before either half's P
             s_hmax[((t & 1) * 2 + h) * 128 + r] = mt;
-            ok = named_bar_and(kBarSoftmax, 256, ready && !*s_abort);
+            ok = named_bar_and(kBarRows0 + (warp & 3), 64, ready && !*s_abort);
             float alpha = 1.f;
             if (ok) {
                 mt = fmaxf(mt, s_hmax[((t & 1) * 2 + (h ^ 1)) * 128 + r]);
@@ -736,7 +738,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         // the second half hands its partial sum to the first, which works out the output
         // factor f = e^{(1-beta) M} Z'^{-beta} and the refusal; both halves then write O
         if (h == 1) s_zpart[r] = Zs + chk;  // chk is 0, or NaN to refuse
-        ok = named_bar_and(kBarSoftmax, 256, ok && !*s_abort);
+        ok = named_bar_and(kBarRows0 + (warp & 3), 64, ok && !*s_abort);
         if (h == 0) {
             Zs += s_zpart[r];
             bool bad = false;
@@ -752,7 +754,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         {
             const int t = numkv, sb = t % L::NSB;
             bool done = ok && wait_bar_warp(B.pv_done + sb, (t / L::NSB) & 1, s_abort, a.status);
-            done = named_bar_and(kBarSoftmax, 256, done);  // also publishes f
+            done = named_bar_and(kBarRows0 + (warp & 3), 64, done);  // also publishes f
             const float f = s_zpart[r];
             constexpr int nq = DVP / 32;  // 32-column chunks; half h writes chunks [h nq/2, (h+1) nq/2)
             if (done) {
