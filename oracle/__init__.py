@@ -81,6 +81,11 @@ def lib():
             L.ro_chain_heads.argtypes = [_f32p, _f32p, _f64p, _f32p, _i64, _i64, _i64, _f64p,
                                          _f64p, _f64p, _i32p, ctypes.c_int]
             L.ro_chain_heads.restype = ctypes.c_int
+            L.ro_position_head.argtypes = [_f32p, _f32p, _i64, _i64, _f64, _f64, _f64p]
+            L.ro_position_head.restype = ctypes.c_int
+            L.ro_position_heads.argtypes = [_f32p, _f32p, _i64, _i64, _i64, _i64, _f64p, _f64p,
+                                            _f64p, _i32p, ctypes.c_int]
+            L.ro_position_heads.restype = ctypes.c_int
             L.ro_max_threads.argtypes = []
             L.ro_max_threads.restype = ctypes.c_int
             _lib = L
@@ -257,3 +262,36 @@ def chain_heads(u, theta, g, b, threads: int = 0):
     if rc == RO_SHAPE:
         raise ShapeError()
     return yr + 1j * yi, env, st
+
+
+def position_head(a, v, beta: float, qk: float) -> np.ndarray:
+    """O [n,dv] real of one position-only head: logits qk * a(i - j) (a [n], one per offset),
+    v [n,dv] (proofs.blah.dev's theorem pos-head-is-causal-convolution, left-hand side, with
+    the switches at g = 0)."""
+    aa, pa = _f32(a)
+    va, pv = _f32(v)
+    n = aa.size
+    if va.ndim != 2 or va.shape[0] != n:
+        raise ShapeError()
+    O = np.zeros((n, va.shape[1]))
+    _raise(lib().ro_position_head(pa, pv, n, va.shape[1], float(beta), float(qk), _ptr64(O)))
+    return O
+
+
+def position_heads(a, v, beta, qk, threads: int = 0):
+    """Position-only heads: a [H,n] (head h of every batch reads row h), v [BH,n,dv];
+    beta/qk scalars or [BH]. Returns (O [BH,n,dv], status [BH])."""
+    aa, pa = _f32(a)
+    va, pv = _f32(v)
+    BH, n, dv = va.shape
+    H = aa.shape[0]
+    if aa.ndim != 2 or aa.shape[1] != n:
+        raise ShapeError()
+    b_, pb_ = _f64a(_per_head(beta, BH)); q_, pq_ = _f64a(_per_head(qk, BH))
+    O = np.zeros((BH, n, dv))
+    st = np.zeros(BH, dtype=np.int32)
+    rc = lib().ro_position_heads(pa, pv, BH, H, n, dv, pb_, pq_, _ptr64(O),
+                                 st.ctypes.data_as(_i32p), int(threads))
+    if rc == RO_SHAPE:
+        raise ShapeError()
+    return O, st

@@ -404,3 +404,58 @@ int ro_chain_heads(const float *u, const float *theta, const double *g, const fl
         if (status[h] != RO_OK) rc = status[h];
     return rc;
 }
+
+/* Position-only head: the definition row by row (see the header). */
+int ro_position_head(const float *a, const float *v, int64_t n, int64_t dv, double beta,
+                     double qk, double *O)
+{
+    if (n == 0) return RO_OK;
+    if (n < 0 || dv <= 0) return RO_SHAPE;
+    if (!isfinite(beta) || !isfinite(qk)) return RO_NONFINITE;
+    if (!all_finite(a, n)) return RO_NONFINITE;
+    double *t = (double *)malloc(sizeof(double) * n);
+    if (!t) return RO_SHAPE;
+    for (int64_t d = 0; d < n; ++d) {
+        t[d] = qk * (double)a[d];  /* the logit of every pair at offset d */
+        if (!isfinite(t[d])) {
+            free(t);
+            return RO_NONFINITE;
+        }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        /* log Z_i from the sum shifted by the row maximum (every entry is live) */
+        double M = -INFINITY;
+        for (int64_t j = 0; j <= i; ++j)
+            if (t[i - j] > M) M = t[i - j];
+        double Zs = 0.0;
+        for (int64_t j = 0; j <= i; ++j) Zs += exp(t[i - j] - M);
+        const double logZ = M + log(Zs);
+        for (int64_t c = 0; c < dv; ++c) O[i * dv + c] = 0.0;
+        for (int64_t j = 0; j <= i; ++j) {
+            const double w = exp(t[i - j] - (beta == 0.0 ? 0.0 : beta * logZ));
+            for (int64_t c = 0; c < dv; ++c) O[i * dv + c] += w * (double)v[j * dv + c];
+        }
+    }
+    free(t);
+    return RO_OK;
+}
+
+int ro_position_heads(const float *a, const float *v, int64_t BH, int64_t H, int64_t n,
+                      int64_t dv, const double *beta, const double *qk, double *O,
+                      int32_t *status, int threads)
+{
+    if (BH < 0 || H <= 0 || n < 0 || dv <= 0) return RO_SHAPE;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#else
+    (void)threads;
+#endif
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t h = 0; h < BH; ++h)
+        status[h] = ro_position_head(a + (h % H) * n, v + h * n * dv, n, dv, beta[h], qk[h],
+                                     O + h * n * dv);
+    int rc = RO_OK;
+    for (int64_t h = 0; h < BH; ++h)
+        if (status[h] != RO_OK) rc = status[h];
+    return rc;
+}

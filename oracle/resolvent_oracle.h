@@ -97,6 +97,25 @@ int ro_chain_heads(const float *u, const float *theta, const double *g, const fl
 /* Threads the OpenMP runtime would use (1 when built without OpenMP). */
 int ro_max_threads(void);
 
+/* Position-only head: "A position-only causal softmax head is a causal convolution divided
+ * by a prefix normalizer" (proofs.blah.dev, theorem pos-head-is-causal-convolution), its
+ * left-hand side, with the switches of "Resolvent Operator" at g = 0 (no gates, so every
+ * entry is live): the logit of query i and key j is t_ij = qk * a(i - j),
+ * W_ij = e^{t_ij} / Z_i^beta with Z_i = sum_{j<=i} e^{t_ij}, evaluated in the log domain of
+ * "Evaluation and refusals" (log Z_i = M_i + log sum_j e^{t_ij - M_i}, M_i = max_j t_ij), and
+ * O_i = sum_{j<=i} W_ij v_j. a [n] (one logit per offset d = i - j), v [n,dv], O [n,dv], all
+ * real. Refusals: a non-finite a(d) for d < n (even at qk = 0, as q and k are refused there),
+ * a non-finite switch, a non-finite qk * a(d). */
+int ro_position_head(const float *a, const float *v, int64_t n, int64_t dv, double beta,
+                     double qk, double *O);
+
+/* The same for BH heads: head h reads its offset logits at a + (h % H) * n (a [H,n], one
+ * table per head index, shared across the batch), v [BH,n,dv], switches beta[h], qk[h];
+ * O [BH,n,dv]. status[h] receives the head's code. Parallel over heads with OpenMP. */
+int ro_position_heads(const float *a, const float *v, int64_t BH, int64_t H, int64_t n,
+                      int64_t dv, const double *beta, const double *qk, double *O,
+                      int32_t *status, int threads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -459,6 +459,85 @@ def test_position_only_head_is_a_causal_convolution(oracle_mod):
     assert np.all(O.imag == 0)
 
 
+def _offset_qk(n, c0, c1, c2):
+    """q, k [n,4] with <q_i, k_j> / sqrt(4) = (c0 + c1 (i-j) + c2 (i-j)^2) / 2 exactly (fp32
+    and fp64 alike for small dyadic c and n), and the same logits per offset d."""
+    i = np.arange(n, dtype=np.float64)
+    q = np.stack([np.ones(n), i, i * i, np.zeros(n)], axis=1).astype(np.float32)
+    k = np.stack([c0 - c1 * i + c2 * i * i, c1 - 2 * c2 * i, np.full(n, c2), np.zeros(n)],
+                 axis=1).astype(np.float32)
+    d = np.arange(n, dtype=np.float64)
+    return q, k, ((c0 + c1 * d + c2 * d * d) / 2.0).astype(np.float32)
+
+
+@pytest.mark.parametrize("beta,qk", [(1.0, 1.0), (0.0, 1.0), (1.0, -0.75), (0.0, 0.5)])
+def test_position_head_is_the_operator_with_offset_logits(oracle_mod, beta, qk):
+    """The position-only head equals the general operator (pinned above) followed by the
+    readout, at g = 0, when <q_i, k_j>/sqrt(d) depends only on i - j."""
+    n = 48
+    q, k, a = _offset_qk(n, 0.5, 0.125, -0.015625)
+    v = rng(31).standard_normal((n, 3)).astype(np.float32)
+    u = np.ones(n, np.float32); th = np.zeros(n, np.float32)
+    ref = oracle_mod.readout(oracle_mod.operator(q, k, u, th, beta, qk, 0.0), v)
+    O = oracle_mod.position_head(a, v, beta, qk)
+    assert np.max(np.abs(O - ref.real)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+    assert np.all(ref.imag == 0)
+
+
+def test_position_head_is_a_causal_convolution_over_a_prefix_sum(oracle_mod):
+    """The theorem's right-hand side: (sum_d e^{a(d)} v_{i-d}) / (sum_{d<=i} e^{a(d)}),
+    by numpy's convolution and cumulative sum."""
+    n = 64
+    a = rng(32).standard_normal(n).astype(np.float32)
+    v = rng(33).standard_normal((n, 4)).astype(np.float32)
+    O = oracle_mod.position_head(a, v, 1.0, 1.0)
+    ea = np.exp(a.astype(np.float64))
+    for ch in range(4):
+        ref = np.convolve(ea, v[:, ch].astype(np.float64))[:n] / np.cumsum(ea)
+        assert np.max(np.abs(O[:, ch] - ref)) <= 1e-13
+
+
+def test_position_head_closed_forms(oracle_mod):
+    """Constant logits: a prefix mean at beta = 1, e^{qk c} times a prefix sum at beta = 0;
+    qk = 0 ignores a entirely."""
+    n = 30
+    v = rng(34).standard_normal((n, 2)).astype(np.float32).astype(np.float64)
+    cnt = np.arange(1, n + 1)[:, None]
+    c = np.full(n, 0.75, np.float32)
+    assert np.max(np.abs(oracle_mod.position_head(c, v, 1.0, 2.0) - np.cumsum(v, 0) / cnt)) <= 1e-13
+    assert np.max(np.abs(oracle_mod.position_head(c, v, 0.0, 2.0) - math.exp(1.5) * np.cumsum(v, 0))) <= 1e-12
+    a = rng(35).standard_normal(n).astype(np.float32)
+    assert np.max(np.abs(oracle_mod.position_head(a, v, 1.0, 0.0) - np.cumsum(v, 0) / cnt)) <= 1e-13
+    # causality: row i reads v_0 .. v_i only
+    O = oracle_mod.position_head(a, v, 1.0, 1.0)
+    v2 = v.copy(); v2[17:] += 5.0
+    O2 = oracle_mod.position_head(a, v2, 1.0, 1.0)
+    assert np.array_equal(O[:17], O2[:17]) and not np.array_equal(O[17:], O2[17:])
+
+
+def test_position_head_refusals_and_batching(oracle_mod):
+    n = 12
+    v = rng(36).standard_normal((n, 2)).astype(np.float32)
+    a = rng(37).standard_normal(n).astype(np.float32)
+    bad = a.copy(); bad[5] = np.inf
+    with pytest.raises(oracle_mod.NonFinite):
+        oracle_mod.position_head(bad, v, 1.0, 0.0)       # refused even at qk = 0
+    big = np.full(n, 1e10, np.float32)
+    with pytest.raises(oracle_mod.NonFinite):
+        oracle_mod.position_head(big, v, 1.0, 1e300)     # qk * a overflows
+    assert oracle_mod.position_head(np.zeros(0, np.float32), np.zeros((0, 2), np.float32),
+                                    1.0, 1.0).shape == (0, 2)
+    # batched: head h of every batch reads table h; per-head switches
+    H, B = 2, 3
+    tab = rng(38).standard_normal((H, n)).astype(np.float32)
+    vv = rng(39).standard_normal((B * H, n, 2)).astype(np.float32)
+    beta = np.array([1.0, 0.0] * B); qk = np.array([1.0, 0.5] * B)
+    O, st = oracle_mod.position_heads(tab, vv, beta, qk)
+    assert np.all(st == 0)
+    for h in range(B * H):
+        assert np.array_equal(O[h], oracle_mod.position_head(tab[h % H], vv[h], beta[h], qk[h]))
+
+
 # ------------------------------------------------------------------ batched routines
 
 
