@@ -76,6 +76,11 @@ def lib() -> ctypes.CDLL:
         L.resolvent_operator.argtypes = [_P, _P, _P, _P, _Switches, _I, _I, _I, _I, _I, _P, _P, _P,
                                          _SZ, _P, _P]
         L.resolvent_operator.restype = _I
+        L.resolvent_position_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+        L.resolvent_position_workspace_bytes.restype = _SZ
+        L.resolvent_position_head.argtypes = [_P, _P, _Switches, _I, _I, _I, _I, _I, _P, _P, _SZ,
+                                              _P, _P]
+        L.resolvent_position_head.restype = _I
         L.resolvent_chain_workspace_bytes.argtypes = [_I, _I, _I, _I]
         L.resolvent_chain_workspace_bytes.restype = _SZ
         L.resolvent_chain_scan.argtypes = [_P, _P, _Switches, _P, _I, _I, _I, _I, _P, _P, _P, _SZ,
@@ -298,6 +303,40 @@ def operator(q, k, u, theta, beta: Switch, qk: Switch, g: Switch, *, out=None, w
     _raise(lib().resolvent_operator(_ptr(q), _ptr(k), _ptr(u), _ptr(theta), sw, B, H, n, d, dt,
                                     _ptr(out[0]), _ptr(out[1]), _ptr(workspace), workspace.numel(),
                                     _ptr(st), _stream(stream)))
+    if sync and status is None:
+        status_sync(st, stream)
+    return out
+
+
+def position_workspace_bytes(B, H, n, dv, dtype: torch.dtype) -> int:
+    return int(lib().resolvent_position_workspace_bytes(
+        B, H, n, dv, RS_F32 if dtype == torch.float32 else RS_BF16))
+
+
+def position_head(a, v, beta: Switch, qk: Switch, *, out=None, workspace=None, status=None,
+                  stream=None, sync: bool = True):
+    """O [B,H,n,dv] fp32 of position-only heads: logits qk * a[h, i - j] (a [H,n] fp32);
+    v [B,H,n,dv] bf16 or fp32; g = 0 ("A position-only causal softmax head is a causal
+    convolution divided by a prefix normalizer")."""
+    if v.dtype not in (torch.bfloat16, torch.float32):
+        raise ResolventError(RS_ERR_UNSUPPORTED, "v must be bf16 or fp32")
+    dt = RS_F32 if v.dtype == torch.float32 else RS_BF16
+    v = _dev(v, "v")
+    a = _dev(a, "a", torch.float32)
+    B, H, n, dv = v.shape
+    if a.shape != (H, n):
+        raise ResolventError(RS_ERR_SHAPE, "a must be [H, n]")
+    sw, keep = _switches(H, beta, qk, 0.0)
+    dev = v.device
+    if out is None:
+        out = torch.empty(B, H, n, dv, device=dev)
+    wsb = int(lib().resolvent_position_workspace_bytes(B, H, n, dv, dt))
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    st = status if status is not None else new_status(dev)
+    _raise(lib().resolvent_position_head(_ptr(a), _ptr(v), sw, B, H, n, dv, dt, _ptr(out),
+                                         _ptr(workspace), workspace.numel(), _ptr(st),
+                                         _stream(stream)))
     if sync and status is None:
         status_sync(st, stream)
     return out

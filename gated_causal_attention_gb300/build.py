@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libresolvent.so")
-SOURCES = ["api.cu", "gate_prep.cu", "chain_scan.cu", "head_fwd.cu", "operator.cu"]
+SOURCES = ["api.cu", "gate_prep.cu", "chain_scan.cu", "head_fwd.cu", "operator.cu", "position.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -510,6 +510,86 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
     return RS_OK;
 }
 
+// Workspace of resolvent_position_head.
+struct PositionWs {
+    size_t vpad, kap, C, meta, total;
+    bool copy_v;
+};
+
+PositionWs position_ws(int B, int H, int n, int dv, rs_dtype dt)
+{
+    PositionWs w{};
+    const size_t BH = (size_t)B * H, tok = BH * n;
+    const size_t slots = std::min<size_t>(BH, kMaxSlots);
+    w.copy_v = dt == RS_F32 || dv != pad64(dv);
+    size_t off = 0;
+    w.vpad = off; off += w.copy_v ? up256(tok * pad64(dv) * 2) : 0;
+    w.kap = off; off += up256(slots * n * 2);
+    w.C = off; off += up256(slots * n * 4);
+    w.meta = off; off += up256(slots * 8);
+    w.total = off;
+    return w;
+}
+
+size_t resolvent_position_workspace_bytes(int B, int H, int n, int dv, rs_dtype dtype)
+{
+    if (B <= 0 || H <= 0 || n <= 0 || dv <= 0) return 0;
+    return position_ws(B, H, n, dv, dtype).total;
+}
+
+rs_status resolvent_position_head(const float *a, const void *v, rs_switches sw, int B, int H, int n,
+                                  int dv, rs_dtype dtype, float *O, void *workspace,
+                                  size_t workspace_bytes, int32_t *status_dev, void *stream)
+{
+    g_launches = 0;
+    if (B < 0 || H < 0 || n < 0) return RS_ERR_SHAPE;
+    if ((size_t)B * H == 0 || n == 0) return RS_OK;
+    if (dv <= 0) return RS_ERR_SHAPE;
+    if (dv > 128) return RS_ERR_UNSUPPORTED;
+    if (dtype != RS_F32 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED;
+    rs_status st = check_switches(sw, H);
+    if (st != RS_OK) return st;
+    for (int h = 0; h < H; ++h)  // the position-only form has no gates
+        if (sw_of(sw, h).g != 0.f) return RS_ERR_UNSUPPORTED;
+    if (!a || !v || !O || !status_dev) return RS_ERR_SHAPE;
+    for (const void *p : {(const void *)a, v, (const void *)O, (const void *)workspace})
+        if (!aligned16(p)) return RS_ERR_ALIGN;
+    const PositionWs w = position_ws(B, H, n, dv, dtype);
+    if (!workspace || workspace_bytes < w.total) return RS_ERR_WORKSPACE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    const int BH = B * H, DVP = pad64(dv);
+    const bool f32 = dtype == RS_F32;
+    const void *vs = v;
+    if (w.copy_v) {
+        __nv_bfloat16 *vp = reinterpret_cast<__nv_bfloat16 *>(ws + w.vpad);
+        if (launch_pad_to_bf16(v, f32, (int64_t)BH * n, dv, vp, DVP, status_dev, 0, s) != cudaSuccess)
+            return RS_ERR_CUDA;
+        g_launches += 1;
+        vs = vp;
+    }
+    PosMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!make_tmap(&maps.v, vs, DVP, n, BH)) return RS_ERR_CUDA;
+    for (const HeadTable &t : tables_for(sw, B, H, [](const Sw &) { return true; })) {
+        PosArgs pa{};
+        pa.n = n; pa.H = H; pa.dv = dv; pa.a = a;
+        pa.kap = reinterpret_cast<__nv_bfloat16 *>(ws + w.kap);
+        pa.C = reinterpret_cast<float *>(ws + w.C);
+        pa.meta = reinterpret_cast<float2 *>(ws + w.meta);
+        pa.O = O; pa.status = status_dev; pa.vec_out = dv % 4 == 0 ? 1 : 0;
+        // about 24 MB of V per head group: a group's V tiles stay in L2
+        const size_t v_head = (size_t)n * DVP * 2;
+        pa.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / v_head));
+        prof_mark(s, 0);
+        if (launch_position_head(pa, t, maps, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
+        prof_mark(s, 1);
+        g_launches += 2;
+    }
+    return RS_OK;
+}
+
 size_t resolvent_chain_workspace_bytes(int B, int H, int n, int dv)
 {
     if (B <= 0 || H <= 0 || n <= 0 || dv <= 0) return 0;

@@ -1,0 +1,384 @@
+// position.cu -- position-only heads as a causal convolution over a prefix normaliser (K5).
+//
+// "A position-only causal softmax head is a causal convolution divided by a prefix
+// normalizer" (proofs.blah.dev, theorem pos-head-is-causal-convolution), with the switches
+// of "Resolvent Operator" at g = 0: when the logit of query i and key j is qk * a(i - j),
+//     O_i = sum_{j<=i} e^{qk a(i-j)} v_j / Z_i^beta,  Z_i = sum_{d<=i} e^{qk a(d)},
+// i.e. a causal convolution of v with the kernel e^{qk a(d)}, over a prefix sum of the same
+// kernel. Two launches per table of heads:
+//   prep  -- one CTA per head: M = max_d qk a(d); kappa(d) = e^{qk a(d) - M} rounded to bf16
+//            (the tensor-core operand); C(i) = sum_{d<=i} kappa(d) over the rounded values, so
+//            that the weights of a row sum to exactly what divides them; and the last offset
+//            whose kappa is not 0;
+//   main  -- one CTA per 128-row query tile: O_tile = sum_delta P(delta) V(QB - delta), P(delta)
+//            the 128 x 128 block-Toeplitz tile P[r][c] = kappa(128 delta + r - c) (0 for a
+//            negative offset or one past n). Builder warps write P into TMEM from a segment of
+//            kappa staged in shared memory (no logits, no exponential per entry); one thread
+//            issues P V (tcgen05.mma, P from TMEM, V by TMA); tiles whose offsets all lie past
+//            the last nonzero kappa are skipped. The epilogue divides by C(i)^beta, multiplies
+//            by e^{(1-beta) M}, and writes O with coalesced 16-byte stores.
+#include "head_common.cuh"
+
+namespace rs {
+
+namespace {
+
+using namespace head;
+
+constexpr int kPrepThreads = 1024;
+
+// One head per CTA. kap_bf16, C: [slots][n]; meta: [slots] = (M, last nonzero offset as a
+// float-coded int) -- written as float2 (M, bit pattern of the offset).
+__global__ void __launch_bounds__(kPrepThreads)
+position_prep_kernel(PosArgs a, const __grid_constant__ HeadTable tab)
+{
+    __shared__ float s_red[32];
+    __shared__ int s_bad, s_dmax;
+    __shared__ float s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slot = blockIdx.x, n = a.n;
+    const float qk = tab.qk[slot];
+    const float *av = a.a + (int64_t)(tab.bh[slot] % a.H) * n;
+    __nv_bfloat16 *kap = a.kap + (int64_t)slot * n;
+    float *C = a.C + (int64_t)slot * n;
+    if (tid == 0) {
+        s_bad = 0;
+        s_dmax = -1;
+        s_carry = 0.f;
+    }
+    // the largest logit, and the refusal of a non-finite a(d) or qk a(d)
+    float mx = -INFINITY;
+    bool bad = false;
+    for (int d = tid; d < n; d += kPrepThreads) {
+        const float x = av[d];
+        const float t = qk * x;
+        bad |= !isfinite(x) || !isfinite(t);
+        mx = fmaxf(mx, t);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_red[warp] = mx;
+    if (__syncthreads_or(bad) && tid == 0) s_bad = 1;
+    if (warp == 0) {
+        float m = s_red[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) s_red[0] = m;
+    }
+    __syncthreads();
+    const float M = s_red[0];
+    if (s_bad) {  // refused: the main launch then builds no tile beyond the first
+        if (tid == 0) {
+            flag_status(a.status, RS_STATUS_NONFINITE_BIT);
+            a.meta[slot] = make_float2(0.f, __int_as_float(-1));
+        }
+        for (int d = tid; d < n; d += kPrepThreads) {
+            kap[d] = __float2bfloat16_rn(0.f);
+            C[d] = 0.f;
+        }
+        return;
+    }
+    // kappa rounded to bf16, its inclusive prefix sum, the last nonzero offset
+    for (int base = 0; base < n; base += kPrepThreads) {
+        const int d = base + tid;
+        float k = 0.f;
+        if (d < n) {
+            const __nv_bfloat16 kb = __float2bfloat16_rn(expf(qk * av[d] - M));
+            kap[d] = kb;
+            k = __bfloat162float(kb);
+            if (k > 0.f) atomicMax(&s_dmax, d);
+        }
+        // block-wide inclusive scan: within warps, then over the warp totals
+        float x = k;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();  // s_red is reused
+        if (lane == 31) s_red[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            float w = s_red[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            s_red[lane] = w;
+        }
+        __syncthreads();
+        const float carry = s_carry;
+        const float incl = carry + (warp > 0 ? s_red[warp - 1] : 0.f) + x;
+        if (d < n) C[d] = incl;
+        __syncthreads();
+        if (tid == kPrepThreads - 1) s_carry = incl;
+    }
+    __syncthreads();
+    if (tid == 0) a.meta[slot] = make_float2(M, __int_as_float(s_dmax));
+}
+
+template <int DVP>
+struct PosCfg {
+    static constexpr uint32_t v_bytes = (DVP / 64) * kRegion;  // one V tile: 128 keys x DVP bf16
+    static constexpr int NSV = 4;                              // V stages
+    static constexpr int NPB = 3;                              // P buffers in TMEM (64 columns each)
+    static constexpr uint32_t ring = 0;
+    static constexpr uint32_t seg = ring + NSV * v_bytes;      // bf16 [NPB][256] kappa segments
+    static constexpr uint32_t rowf = seg + NPB * 512;          // float [128] row factors
+    static constexpr uint32_t bars = rowf + 512;               // vfull, vempty, pfull, pfree, accfull
+    static constexpr int nbars = 2 * NSV + 2 * NPB + 1;
+    static constexpr uint32_t misc = bars + nbars * 8;         // tmem slot, abort flag
+    static constexpr uint32_t end = misc + 16;
+    static constexpr uint32_t alloc = end + 1024;
+    static constexpr uint32_t p_col0 = DVP;                    // TMEM: accumulator, then P buffers
+    static_assert(DVP + NPB * 64 <= 512, "TMEM budget");
+    static_assert((DVP / 32) * kRegion <= NSV * v_bytes, "epilogue staging in the V ring");
+    static_assert(alloc <= 227 * 1024, "shared memory");
+};
+
+constexpr int kPosThreads = 384;  // warpgroup 0: TMA (warp 0) and MMA (warp 1); 1-2: P builders
+constexpr int kBarBuild = 1;
+
+template <int DVP>
+__global__ void __launch_bounds__(kPosThreads, 1)
+position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __grid_constant__ PosMaps maps)
+{
+    using L = PosCfg<DVP>;
+    constexpr int NSV = L::NSV, NPB = L::NPB;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *vfull = reinterpret_cast<uint64_t *>(smem + L::bars);
+    uint64_t *vempty = vfull + NSV, *pfull = vfull + 2 * NSV, *pfree = pfull + NPB, *accfull = pfree + NPB;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L::misc) + 1;
+    float *s_rowf = reinterpret_cast<float *>(smem + L::rowf);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
+    const int n = a.n, nqt = (n + 127) / 128;
+    // blocks run head group by head group (a group's V stays in L2 while its query tiles
+    // stream it), longest query tiles first within a group
+    const int G = a.heads_per_group;
+    const int grp = (int)blockIdx.x / (G * nqt);
+    const int rem = (int)blockIdx.x - grp * G * nqt;
+    const int gsz = min(G, tab.count - grp * G);
+    const int QB = nqt - 1 - rem / gsz;
+    const int slot = grp * G + rem % gsz;
+    const int bh = tab.bh[slot];
+    const float2 meta = a.meta[slot];  // (M, last offset whose kappa is not 0)
+    const int dmax = __float_as_int(meta.y);
+    // block offsets delta = 0 .. T-1 (key tile QB - delta); past the last nonzero kappa every
+    // entry of P(delta) is 0
+    const int T = min(QB, max((dmax + 127) / 128, 0)) + 1;
+
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < L::nbars; ++i) mbar_init(vfull + i, 1);
+        for (int i = 0; i < NPB; ++i) mbar_init(pfull + i, 8);  // one arrival per builder warp
+        *s_abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&maps.v);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (wg == 0) {
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA: V tiles
+            for (int t = 0; t < T; ++t) {
+                const int sv = t % NSV;
+                if (t >= NSV && !wait_bar(vempty + sv, ((t / NSV) - 1) & 1, s_abort, a.status, 256)) break;
+                unsigned char *stg = smem + L::ring + sv * L::v_bytes;
+                mbar_arrive_expect_tx(vfull + sv, L::v_bytes);
+                for (int rr = 0; rr < DVP / 64; ++rr)
+                    tma_load_3d(stg + rr * kRegion, &maps.v, vfull + sv, rr * 64, (QB - t) * 128, bh);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA: O += P V
+            constexpr uint32_t idesc = idesc_bf16(128, DVP, false, true);
+            const uint64_t dv0 = sw128_desc(sbase + L::ring, kRegion, 1024);
+            bool ok = true;
+            for (int t = 0; t < T; ++t) {
+                const int pb = t % NPB, sv = t % NSV;
+                if (!wait_bar(pfull + pb, (t / NPB) & 1, s_abort, a.status, 32) ||
+                    !wait_bar(vfull + sv, (t / NSV) & 1, s_abort, a.status, 32)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t pcol = tmem + L::p_col0 + pb * 64;
+                const uint64_t dv = dv0 + (((uint32_t)sv * L::v_bytes) >> 4);
+                umma_bf16_ts(tmem, pcol, dv, idesc, t > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 1; ks < 8; ++ks) umma_bf16_ts(tmem, pcol + ks * 8, dv + (ks * 2048 >> 4), idesc, 1u);
+                umma_commit(pfree + pb);
+                umma_commit(vempty + sv);
+            }
+            if (ok) umma_commit(accfull);
+        }
+    } else {
+        // ------------------------------------------------------------ P builders
+        // Thread (h, r): row r of every P(delta), keys [64h, 64h + 64). The kappa segment of
+        // block offset delta, seg[e] = kappa(128 delta - 128 + e) (0 outside [0, n)), is staged
+        // by all 256 builders; key c of row r is seg[r - c + 128].
+        const int h = wg - 1, r = tid & 127, bt = tid - 128;  // bt: 0..255 over the builders
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const __nv_bfloat16 *kap = a.kap + (int64_t)slot * n;
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int pb = t % NPB;
+            // buffer pb last held P(t - NPB): its MMA (and so every builder's reads of the
+            // segment, which came before the builders' arrivals) is done
+            if (ok && t >= NPB) ok = wait_bar_warp(pfree + pb, ((t / NPB) - 1) & 1, s_abort, a.status, 0);
+            unsigned short *seg = reinterpret_cast<unsigned short *>(smem + L::seg + pb * 512);
+            {
+                const int off = 128 * t - 128 + bt;
+                unsigned short v = 0;
+                if (off >= 0 && off < n) v = __bfloat16_as_ushort(kap[off]);
+                seg[bt] = v;
+            }
+            ok = named_bar_and(kBarBuild, 256, ok && !*s_abort);
+            if (!ok) break;
+            // key pair (c, c+1), c = 64h + 2p: low half seg[e0 + 1], high half seg[e0] with
+            // e0 = r - c + 127. Its parity is that of r + 1 for every pair of the row.
+            const uint32_t *seg32 = reinterpret_cast<const uint32_t *>(seg);
+            uint32_t pk[32];
+            const int e0top = r - 64 * h + 127;  // e0 of the first pair; each next pair is 2 lower
+            if (e0top & 1) {
+                // e0 odd: the pair straddles words (e0 - 1)/2 (high half) and (e0 + 1)/2 (low half)
+                uint32_t wb = seg32[(e0top + 1) >> 1];
+#pragma unroll
+                for (int p = 0; p < 32; ++p) {
+                    const uint32_t wa = seg32[((e0top - 2 * p) - 1) >> 1];
+                    pk[p] = __byte_perm(wb, wa, 0x7610);
+                    wb = wa;
+                }
+            } else {
+                // e0 even: word e0/2 holds (seg[e0], seg[e0 + 1]); swap its halves
+#pragma unroll
+                for (int p = 0; p < 32; ++p) {
+                    const uint32_t w = seg32[(e0top - 2 * p) >> 1];
+                    pk[p] = __byte_perm(w, 0u, 0x1032);
+                }
+            }
+            const uint32_t pc = trow + L::p_col0 + pb * 64 + 32 * h;
+            RS_TMEM_ST16(pc, pk);
+            RS_TMEM_ST16(pc + 16, (pk + 16));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull + pb);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0
+        const int row = QB * 128 + r;
+        const bool valid = row < n;
+        if (h == 0) {
+            const float beta = tab.beta[slot], M = meta.x;
+            float f = 0.f;
+            bool bad = false;
+            if (valid) {
+                const float Ci = a.C[(int64_t)slot * n + row];
+                bad = !(Ci > 0.f);  // every kappa of the row underflowed
+                f = (beta == 0.f) ? expf(M) : expf((1.f - beta) * M - beta * logf(Ci));
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
+            s_rowf[r] = f;
+        }
+        bool done = ok && wait_bar_warp(accfull, 0, s_abort, a.status, 0);
+        done = named_bar_and(kBarBuild, 256, done);  // also publishes the row factors
+        const float f = s_rowf[r];
+        constexpr int nq = DVP / 32;  // 32-column chunks; half h takes [h nq/2, (h+1) nq/2)
+        const uint32_t stage = sbase + L::ring;
+        if (done) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = h * nq / 2; q < (h + 1) * nq / 2; ++q) {
+                uint32_t acc[32];
+                RS_TMEM_LD32(trow + 32 * q, acc);  // warp-wide: every lane, valid row or not
+                tmem_ld_wait();
+                if (a.vec_out) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float x = __uint_as_float(acc[4 * c + k]);
+                            w[k] = __float_as_uint(x == 0.f ? 0.f : x * f);
+                        }
+                        sts128(stage + q * kRegion + r * 128 + ((c ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+                    }
+                } else if (valid) {  // rows of dv % 4 != 0 floats: plain stores from registers
+                    float *o = a.O + ((int64_t)bh * n + row) * a.dv;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * q + e < a.dv) {
+                            const float x = __uint_as_float(acc[e]);
+                            o[32 * q + e] = x == 0.f ? 0.f : x * f;
+                        }
+                }
+            }
+        }
+        done = named_bar_and(kBarBuild, 256, done);
+        if (done && a.vec_out) {
+            // coalesced 16-byte stores: lane l takes unit l % 8 of row l / 8 of four rows
+            const int wi = bt >> 5, unit = lane & 7;
+            const int nrows = min(128, n - QB * 128);
+            float *o0 = a.O + ((int64_t)bh * n + QB * 128) * a.dv;
+#pragma unroll 1
+            for (int q = 0; q < nq; ++q) {
+                const int col = 32 * q + 4 * unit;
+                if (col >= a.dv) continue;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = 32 * k + 4 * wi + (lane >> 3);
+                    if (rr >= nrows) continue;
+                    const uint4 v = lds128(stage + q * kRegion + rr * 128 + ((unit ^ (rr & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(o0 + (int64_t)rr * a.dv + col) = v;
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int DVP>
+cudaError_t launch_pos(const PosArgs &a, const HeadTable &tab, const PosMaps &maps, cudaStream_t s)
+{
+    using L = PosCfg<DVP>;
+    position_prep_kernel<<<tab.count, kPrepThreads, 0, s>>>(a, tab);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto k = position_head_kernel<DVP>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
+    if (e != cudaSuccess) return e;
+    const int nqt = (a.n + 127) / 128;
+    k<<<nqt * tab.count, kPosThreads, L::alloc, s>>>(a, tab, maps);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_position_head(const PosArgs &a, const HeadTable &tab, const PosMaps &maps, int dvpad,
+                                 cudaStream_t s)
+{
+    if (tab.count == 0 || a.n == 0) return cudaSuccess;
+    return dvpad == 64 ? launch_pos<64>(a, tab, maps, s) : launch_pos<128>(a, tab, maps, s);
+}
+
+}  // namespace rs

@@ -130,6 +130,26 @@ cudaError_t launch_operator_stats(const OpArgs &a, const HeadTable &tab, const O
 cudaError_t launch_operator(const OpArgs &a, const HeadTable &tab, const OpMaps &maps, int dpad,
                             cudaStream_t s);
 
+// ---------------------------------------------------------------- position-only heads (K5)
+struct PosArgs {
+    int n, H, dv;
+    const float *a;              // [H, n] logit per offset d = i - j (head h of every batch reads row h)
+    __nv_bfloat16 *kap;          // [slots, n] kappa(d) = e^{qk a(d) - M} rounded to bf16 (scratch)
+    float *C;                    // [slots, n] prefix sums of the rounded kappa (scratch)
+    float2 *meta;                // [slots] (M, last offset whose kappa is not 0, as int bits)
+    float *O;                    // [BH, n, dv]
+    int32_t *status;
+    int vec_out;                 // O staged and written by 16-byte stores (dv % 4 == 0)
+    int heads_per_group;         // blocks are ordered head group by head group
+};
+// v (bf16, box 64 x 128).
+struct PosMaps {
+    CUtensorMap v;
+};
+// The prep launch (kappa, prefix sums) then the main launch, per table; dvpad in {64, 128}.
+cudaError_t launch_position_head(const PosArgs &a, const HeadTable &tab, const PosMaps &maps, int dvpad,
+                                 cudaStream_t s);
+
 // ---------------------------------------------------------------- debug path product
 cudaError_t launch_debug_path_product(const float2 *gate, const float2 *prefix,
                                       const float2 *suffix, const float2 *carry, int n,

@@ -137,6 +137,29 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
                              float *W_re, float *W_im, void *workspace, size_t workspace_bytes,
                              int32_t *status_dev, void *stream);
 
+/* Workspace bytes resolvent_position_head needs for these sizes (0 when n == 0). */
+size_t resolvent_position_workspace_bytes(int B, int H, int n, int dv, rs_dtype dtype);
+
+/*
+ * Position-only heads: "A position-only causal softmax head is a causal convolution divided
+ * by a prefix normalizer" (proofs.blah.dev, theorem pos-head-is-causal-convolution), with the
+ * switches of "Resolvent Operator" at g = 0. The logit of query i and key j is qk * a_h(i - j):
+ *     O_i = sum_{j<=i} e^{qk a(i-j)} v_j / Z_i^beta,  Z_i = sum_{d<=i} e^{qk a(d)},
+ * evaluated as the theorem's right-hand side: a causal convolution of v with the kernel
+ * kappa(d) = e^{qk a(d) - M} (M the head's largest logit; kappa rounded to bf16 for the tensor
+ * cores) over the prefix sum of the same rounded kernel, times e^{(1-beta) M}. No logit is
+ * formed per entry. a fp32 [H,n] (row h serves head h of every batch); v [B,H,n,dv] bf16
+ * (RS_BF16) or fp32 (RS_F32: rounded to bf16 first); O fp32 [B,H,n,dv] (real: no gates).
+ * beta and qk per head from the switches; every g must be 0 (else RS_ERR_UNSUPPORTED).
+ * Supported: 1 <= dv <= 128. Caller-owned device memory, 16-byte aligned.
+ * Refusals (RS_STATUS_NONFINITE): a non-finite a(d) (even at qk = 0) or qk * a(d), and a row
+ * whose kernel values all underflow in fp32 (logits spread over more than ~87 nats in one
+ * head). Errors as for resolvent_head_forward.
+ */
+rs_status resolvent_position_head(const float *a, const void *v, rs_switches sw, int B, int H,
+                                  int n, int dv, rs_dtype dtype, float *O, void *workspace,
+                                  size_t workspace_bytes, int32_t *status_dev, void *stream);
+
 /* Workspace bytes resolvent_chain_scan needs for these sizes (0 when n == 0). */
 size_t resolvent_chain_workspace_bytes(int B, int H, int n, int dv);
 

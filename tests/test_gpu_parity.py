@@ -458,3 +458,75 @@ def test_operator_rows_are_stochastic(R):
     rows = Wre.double().sum(dim=-1).cpu().numpy()
     assert np.max(np.abs(rows - 1.0)) <= 1e-4
     assert torch.all(Wim == 0)
+
+
+# ------------------------------------------------------------------ position-only heads
+
+POS_CASES = [
+    # B, H, n, dv, dtype, beta, qk, noise, slope_scale
+    (1, 2, 130, 64, "bf16", 1.0, 1.0, 1.0, 0.0),
+    (2, 3, 300, 40, "fp32", 0.0, 0.5, 0.5, 0.05),
+    (1, 2, 257, 37, "bf16", 1.0, -0.75, 1.0, 0.0),
+    (1, 1, 1, 8, "fp32", 1.0, 1.0, 1.0, 0.0),
+    (1, 4, 1024, 128, "bf16", 1.0, 1.0, 0.5, 1.0),
+    (1, 2, 640, 64, "bf16", 0.5, 1.0, 0.5, 0.01),
+]
+
+
+@pytest.mark.parametrize("case", POS_CASES, ids=[str(i) for i in range(len(POS_CASES))])
+def test_position_head_matches_oracle(R, oracle_mod, case):
+    """Position-only heads against the oracle's definition, every entry. Bound: kappa is
+    rounded to bf16 (relative 2^-9) in the convolution and in the prefix normaliser, and v is
+    rounded to bf16 for fp32 inputs, so each output moves by at most about 2^-7 times the
+    same weighted sum of |v| (the oracle run on |v|), plus fp32 accumulation."""
+    B, H, n, dv, dt, beta, qk, noise, slope = case
+    pi = W.position_inputs(B, H, n, dv, seed=700 + n + dv, dtype=dt, noise=noise,
+                           slope_scale=slope, beta=beta, qk=qk)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    O = R.position_head(dev(pi.a), dev(pi.v.reshape(B, H, n, dv), tdt), beta, qk)
+    torch.cuda.synchronize()
+    Og = O.cpu().double().numpy().reshape(B * H, n, dv)
+    bq, qq = [f32(x) for x in pi.switches_bh()]
+    ref, st = oracle_mod.position_heads(pi.a, pi.v, bq, qq)
+    absr, _ = oracle_mod.position_heads(pi.a, np.abs(pi.v), bq, qq)
+    assert np.all(st == 0)
+    err = np.abs(Og - ref)
+    bound = 2.0 ** -7 * absr + 1e-6 * (1.0 + np.max(absr))
+    assert np.all(err <= bound), f"{case}: worst excess {np.max(err - bound)}"
+
+
+def test_position_head_rows_sum_to_one_and_causal(R):
+    """beta = 1 with v = 1 gives exactly the ratio of two sums of the same rounded weights
+    (1 up to fp32 rounding), and a row never reads a later value."""
+    B, H, n, dv = 1, 3, 700, 64
+    pi = W.position_inputs(B, H, n, dv, seed=41, noise=1.0, slope_scale=0.02)
+    ones = torch.ones(B, H, n, dv, dtype=torch.bfloat16, device="cuda")
+    O = R.position_head(dev(pi.a), ones, 1.0, 1.0)
+    assert torch.max(torch.abs(O - 1.0)).item() <= 1e-5
+    v = dev(pi.v.reshape(B, H, n, dv), torch.bfloat16)
+    O1 = R.position_head(dev(pi.a), v, 1.0, 1.0)
+    v2 = v.clone(); v2[:, :, 333:] += 3.0
+    O2 = R.position_head(dev(pi.a), v2, 1.0, 1.0)
+    assert torch.equal(O1[:, :, :333], O2[:, :, :333])
+    assert not torch.equal(O1[:, :, 333:], O2[:, :, 333:])
+
+
+def test_position_head_refusals(R):
+    """Non-finite a (even at qk = 0) and a row whose kernel all underflows are refused; a gate
+    switch other than 0 is not this form."""
+    B, H, n, dv = 1, 2, 200, 64
+    pi = W.position_inputs(B, H, n, dv, seed=42)
+    v = dev(pi.v.reshape(B, H, n, dv), torch.bfloat16)
+    bad = pi.a.copy(); bad[1, 17] = np.nan
+    with pytest.raises(R.NonFinite):
+        R.position_head(dev(bad), v, 1.0, 0.0)
+    spread = np.zeros((H, n), np.float32); spread[:, 0] = -200.0  # row 0 sees only e^{-200 - 0}
+    with pytest.raises(R.NonFinite):
+        R.position_head(dev(spread), v, 1.0, 1.0)
+    with pytest.raises(R.ResolventError):
+        R._raise(R.lib().resolvent_position_head(
+            R._ptr(dev(pi.a)), R._ptr(v), R._switches(H, 1.0, 1.0, 0.5)[0], B, H, n, dv, R.RS_BF16,
+            R._ptr(torch.empty(B, H, n, dv, device="cuda")),
+            R._ptr(torch.empty(R.position_workspace_bytes(B, H, n, dv, torch.bfloat16), dtype=torch.uint8, device="cuda")),
+            R.position_workspace_bytes(B, H, n, dv, torch.bfloat16), R._ptr(R.new_status(torch.device("cuda"))), None))
+

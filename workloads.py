@@ -11,7 +11,7 @@ Generator (counter-based, so any slice can be drawn independently and in paralle
   * normal: Box-Muller on the uniforms of counters 2i and 2i+1 (cosine branch).
 Values are drawn in fp64, rounded to fp32, and then to bf16 (round to nearest even) where
 a workload stores bf16. Seeds: 0x5EED0000 + workload index; streams q=1, k=2, v/b=3, u=4,
-theta=5, positions=6, forced gate values=7.
+theta=5, positions=6, forced gate values=7, position-only logits=8.
 """
 from __future__ import annotations
 
@@ -26,7 +26,7 @@ GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 SEED_BASE = 0x5EED0000
-STREAM = {"q": 1, "k": 2, "v": 3, "b": 3, "u": 4, "theta": 5, "pos": 6, "forced": 7}
+STREAM = {"q": 1, "k": 2, "v": 3, "b": 3, "u": 4, "theta": 5, "pos": 6, "forced": 7, "a": 8}
 _CHUNK = 1 << 22
 
 
@@ -242,6 +242,50 @@ def operator_heads(B=1, H=8, n=4096) -> HeadInputs:
                        name=f"operator B{B} H{H} n{n} d64")
 
 
+@dataclass
+class PositionInputs:
+    """Position-only heads: a [H,n] logit per offset d = i - j (row h serves head h of every
+    batch), v [BH,n,dv] (fp32 arrays holding the stored values), switches beta, qk [H]."""
+    B: int
+    H: int
+    n: int
+    dv: int
+    dtype: str
+    a: np.ndarray
+    v: np.ndarray
+    beta: np.ndarray
+    qk: np.ndarray
+    name: str = ""
+
+    def switches_bh(self):
+        return (np.tile(self.beta, self.B), np.tile(self.qk, self.B))
+
+
+def position_inputs(B, H, n, dv, *, seed, dtype="bf16", noise=0.5, slope_scale=1.0, beta=1.0,
+                    qk=1.0, name="") -> PositionInputs:
+    """a_h(d) = -s_h d + noise * N(0,1) with geometric slopes s_h = slope_scale * 2^{-8(h+1)/H}
+    (one per head, steep to gentle); v ~ N(0,1)."""
+    BH = B * H
+    rnd = (lambda x: to_bf16_values(x)) if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    d = np.arange(n, dtype=np.float64)
+    slopes = slope_scale * 2.0 ** (-8.0 * (np.arange(H) + 1) / H)
+    a = (-slopes[:, None] * d[None, :] + noise * normal(seed, STREAM["a"], H * n).reshape(H, n))
+    v = rnd(normal(seed, STREAM["v"], BH * n * dv).astype(np.float32)).reshape(BH, n, dv)
+
+    def per_head(x):
+        x = np.asarray(x, dtype=np.float64).reshape(-1)
+        return np.full(H, x[0]) if x.size == 1 else x.copy()
+
+    return PositionInputs(B, H, n, dv, dtype, a.astype(np.float32), v, per_head(beta),
+                          per_head(qk), name)
+
+
+def position(B=4, H=32, n=8192) -> PositionInputs:
+    """Position-only heads at the long-softmax shape: B=4 H=32 n=8192 dv=128 bf16 v ~ N(0,1);
+    a_h(d) = -2^{-8(h+1)/32} d + 0.5 N(0,1); (beta, qk) = (1, 1)."""
+    return position_inputs(B, H, n, 128, seed=SEED_BASE + 6, name=f"position B{B} H{H} n{n} dv128")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "gated_softmax": gated_softmax,
@@ -249,4 +293,5 @@ WORKLOADS = {
     "chain": chain,
     "mixed": mixed,
     "operator": operator_heads,
+    "position": position,
 }
