@@ -123,6 +123,20 @@ def head_work(hi: W.HeadInputs):
     return flops, chain_tokens
 
 
+def position_work(pi: W.PositionInputs):
+    """Algorithmic flops of the position-only head: per head, 2 dv per causal entry whose
+    kernel value e^{qk a(d) - M} is not 0 once rounded to bf16 (an offset d contributes
+    n - d entries)."""
+    beta, qk = pi.switches_bh()
+    flops = 0.0
+    cnt = np.arange(pi.n, 0, -1, dtype=np.float64)  # entries at offset d: n - d
+    for h in range(pi.B * pi.H):
+        t = qk[h] * pi.a[h % pi.H].astype(np.float64)
+        live = np.exp(t - t.max()) >= 2.0 ** -134
+        flops += 2 * pi.dv * float(cnt[live].sum())
+    return flops
+
+
 def chain_bytes_per_token(dv, b_bytes=4):
     return b_bytes * dv + 8 + 8 * dv  # read b and (u, theta); write y_re, y_im
 
@@ -185,7 +199,8 @@ class Clocks:
 
 KERNEL_SOURCES = {"head_fwd_kernel": ["head_fwd.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"],
                   "chain_scan_kernel": ["chain_scan.cu", "common.cuh"],
-                  "operator_kernel": ["operator.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"]}
+                  "operator_kernel": ["operator.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"],
+                  "position_head_kernel": ["position.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"]}
 
 
 def measured_traffic(kernel, workload):
@@ -270,6 +285,19 @@ def oracle_sample_operator(hi: W.HeadInputs, target_s: float):
     return heads * hi.n * hi.n / dt, heads * hi.n * hi.n, dt
 
 
+def oracle_sample_position(pi: W.PositionInputs, target_s: float):
+    """The oracle on whole position-only heads: one head (one core) for a short sample,
+    else as many heads as the host has cores, in one parallel pass."""
+    import oracle
+    oracle.build()
+    beta, qk = [np.asarray(x, np.float32).astype(np.float64) for x in pi.switches_bh()]
+    heads = 1 if target_s < 8.0 else max(1, min(pi.B * pi.H, oracle.max_threads()))
+    t0 = time.perf_counter()
+    oracle.position_heads(pi.a, pi.v[:heads], beta[:heads], qk[:heads])
+    dt = time.perf_counter() - t0
+    return heads * pi.n / dt, heads * pi.n, dt
+
+
 def cpu_cores():
     import oracle
     oracle.build()
@@ -280,6 +308,11 @@ def config_of(args, inp, world):
     if isinstance(inp, W.ChainInputs):
         cfg = {"workload": args.workload, "B": inp.B, "H": inp.H, "n": inp.n, "dv": inp.dv,
                "dtype_b": "fp32", "switches": "(0,0,1)"}
+    elif isinstance(inp, W.PositionInputs):
+        sw = sorted({(float(b), float(q)) for b, q in zip(inp.beta, inp.qk)})
+        cfg = {"workload": args.workload, "B": inp.B, "H": inp.H, "n": inp.n, "dv": inp.dv,
+               "dtype_v": inp.dtype, "logits": "a_h(d) = -2^(-8(h+1)/H) d + 0.5 N(0,1)",
+               "switches (beta, qk; g = 0)": sw[0] if len(sw) == 1 else f"{len(sw)} per-head settings"}
     else:
         sw = sorted({(float(b), float(q), float(g)) for b, q, g in zip(inp.beta, inp.qk, inp.g)})
         cfg = {"workload": args.workload, "B": inp.B, "H": inp.H, "n": inp.n, "d": inp.d,
@@ -299,8 +332,11 @@ def run_reference(args):
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup) * 2)
     is_chain = isinstance(inp, W.ChainInputs)
     is_op = args.workload == "operator"
+    is_pos = isinstance(inp, W.PositionInputs)
     if is_chain:
         sample = lambda: oracle_sample_chain(inp, per_step)
+    elif is_pos:
+        sample = lambda: oracle_sample_position(inp, per_step)
     elif is_op:
         sample = lambda: oracle_sample_operator(inp, per_step)
     else:
@@ -317,7 +353,8 @@ def run_reference(args):
     cores = cpu_cores()
     unit = "entries/s" if is_op else "tokens/s"
     metric = ("chain tokens/s (B*H*n/s)" if is_chain else
-              "operator entries/s (B*H*n*n/s)" if is_op else "head tokens/s (B*H*n/s)")
+              "operator entries/s (B*H*n*n/s)" if is_op else
+              "position tokens/s (B*H*n/s)" if is_pos else "head tokens/s (B*H*n/s)")
     line = {"impl": "reference", "metric": metric,
             "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
@@ -326,6 +363,7 @@ def run_reference(args):
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": ("whole heads of the chain" if is_chain else
                                         "whole heads' W" if is_op else
+                                        "whole position-only heads" if is_pos else
                                         "seeded random rows of every head") +
                              f", {toks} {'entries' if is_op else 'tokens'} in {secs:.1f} s"},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
@@ -349,6 +387,7 @@ def run_ours(args):
     inp = make_inputs(args)
     is_chain = isinstance(inp, W.ChainInputs)
     is_op = args.workload == "operator"
+    is_pos = isinstance(inp, W.PositionInputs)
     shp = (inp.B, inp.H, inp.n)
     tdev = lambda x, s, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(
         device=device, dtype=dt)
@@ -374,6 +413,17 @@ def run_ours(args):
         # bytes: W written (8 B per entry); q, k read (2 B x d each per token); u, theta
         work = tokens * 8 + inp.B * inp.H * inp.n * (4 * inp.d + 8)
         host_in = [inp.q, inp.k, inp.u, inp.theta]
+    elif is_pos:
+        a = tdev(inp.a, (inp.H, inp.n))
+        v = tdev(inp.v, (*shp, inp.dv), torch.bfloat16)
+        out = torch.empty(*shp, inp.dv, device=device)
+        ws = torch.empty(max(1, R.position_workspace_bytes(*shp, inp.dv, torch.bfloat16)),
+                         dtype=torch.uint8, device=device)
+        step = lambda: R.position_head(a, v, inp.beta, inp.qk, out=out, workspace=ws, status=status,
+                                       sync=False)
+        tokens = inp.B * inp.H * inp.n
+        work = position_work(inp)
+        host_in = [inp.a, inp.v]
     else:
         dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
         q, k = tdev(inp.q, (*shp, inp.d), dt), tdev(inp.k, (*shp, inp.d), dt)
@@ -433,10 +483,11 @@ def run_ours(args):
                 "kernel_ms": kern, "peak_kind": pk_kind,
                 "algorithmic_bytes_per_launch": work}
     else:
+        kname = "position_head_kernel" if is_pos else "head_fwd_kernel"
         achieved = work / (kern / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16_tflops"],
-                "traffic": measured_traffic("head_fwd_kernel", args.workload), "kernel": "head_fwd_kernel",
+                "traffic": measured_traffic(kname, args.workload), "kernel": kname,
                 "kernel_ms": kern, "peak_kind": pk_kind + " burst",
                 "algorithmic_flops_per_launch": work}
 
@@ -447,11 +498,14 @@ def run_ours(args):
         if is_op:
             pinned[0] = pinned[0].to(torch.bfloat16).pin_memory()
             pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
+        elif is_pos:
+            pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
         elif not is_chain and inp.dtype == "bf16":
             pinned[0] = pinned[0].to(torch.bfloat16).pin_memory()
             pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
             pinned[2] = pinned[2].to(torch.bfloat16).pin_memory()
-        outs_host = [torch.empty(out[0].shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+        outs_host = [torch.empty((out if is_pos else out[0]).shape, dtype=torch.float32).pin_memory()
+                     for _ in range(1 if is_pos else 2)]
         h2d = sum(p.numel() * p.element_size() for p in pinned)
         d2h = sum(o.numel() * o.element_size() for o in outs_host)
 
@@ -466,13 +520,17 @@ def run_ours(args):
                 o = R.operator(qq.view(*shp, inp.d), kk.view(*shp, inp.d), uu.view(shp),
                                tt.view(shp), inp.beta, inp.qk, inp.g, out=out, workspace=ws,
                                status=status, sync=False)
+            elif is_pos:
+                aa, vv = dv_in
+                o = (R.position_head(aa.view(inp.H, inp.n), vv.view(*shp, inp.dv), inp.beta, inp.qk,
+                                     out=out, workspace=ws, status=status, sync=False),)
             else:
                 qq, kk, vv, uu, tt = dv_in
                 o = R.head_forward(qq.view(*shp, inp.d), kk.view(*shp, inp.d), uu.view(shp),
                                    tt.view(shp), vv.view(*shp, inp.dv), inp.beta, inp.qk, inp.g,
                                    out=out, workspace=ws, status=status, sync=False)
-            outs_host[0].copy_(o[0], non_blocking=True)
-            outs_host[1].copy_(o[1], non_blocking=True)
+            for oh, od in zip(outs_host, o):
+                oh.copy_(od, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -493,21 +551,23 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, toks, secs = (oracle_sample_chain(inp, args.cpu_seconds) if is_chain
                             else oracle_sample_operator(inp, args.cpu_seconds) if is_op
+                            else oracle_sample_position(inp, args.cpu_seconds) if is_pos
                             else oracle_sample_head(inp, args.cpu_seconds))
         cpu = {"value": rate, "unit": "entries/s" if is_op else "tokens/s", "cores": cpu_cores(),
                "kind": "oracle",
-               "sample": (f"{toks // inp.n} whole heads" if is_chain else
+               "sample": (f"{toks // inp.n} whole heads" if is_chain or is_pos else
                           f"{toks // (inp.n * inp.n)} whole heads' W" if is_op else
                           f"{toks // (inp.B * inp.H)} seeded random rows of each of the "
                           f"{inp.B * inp.H} heads") + f" ({toks} {'entries' if is_op else 'tokens'}, {secs:.1f} s)"}
 
     if rank == 0:
         line = {"metric": ("chain tokens/s (B*H*n/s)" if is_chain else
-                           "operator entries/s (B*H*n*n/s)" if is_op else "head tokens/s (B*H*n/s)"),
+                           "operator entries/s (B*H*n*n/s)" if is_op else
+                           "position tokens/s (B*H*n/s)" if is_pos else "head tokens/s (B*H*n/s)"),
                 "value": value, "unit": "entries/s" if is_op else "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32" if (is_chain or is_op) else ("bf16" if inp.dtype == "bf16" else "f32->bf16"),
+                "dtype": "f32" if (is_chain or is_op) else "bf16" if is_pos else ("bf16" if inp.dtype == "bf16" else "f32->bf16"),
                 "data": "synthetic (seeded, workloads.py)",
                 "config": dict(config_of(args, inp, world), l2="flushed between timed steps"),
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,

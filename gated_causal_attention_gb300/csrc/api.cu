@@ -510,6 +510,9 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
     return RS_OK;
 }
 
+// Row stride of the position kernel table: whole 128-key tiles, plus one more (zeros).
+int position_kstride(int n) { return (n + 127) / 128 * 128 + 128; }
+
 // Workspace of resolvent_position_head.
 struct PositionWs {
     size_t vpad, kap, C, meta, total;
@@ -524,7 +527,7 @@ PositionWs position_ws(int B, int H, int n, int dv, rs_dtype dt)
     w.copy_v = dt == RS_F32 || dv != pad64(dv);
     size_t off = 0;
     w.vpad = off; off += w.copy_v ? up256(tok * pad64(dv) * 2) : 0;
-    w.kap = off; off += up256(slots * n * 2);
+    w.kap = off; off += up256(slots * (size_t)position_kstride(n) * 2);
     w.C = off; off += up256(slots * n * 4);
     w.meta = off; off += up256(slots * 8);
     w.total = off;
@@ -576,6 +579,7 @@ rs_status resolvent_position_head(const float *a, const void *v, rs_switches sw,
         PosArgs pa{};
         pa.n = n; pa.H = H; pa.dv = dv; pa.a = a;
         pa.kap = reinterpret_cast<__nv_bfloat16 *>(ws + w.kap);
+        pa.kstride = position_kstride(n);
         pa.C = reinterpret_cast<float *>(ws + w.C);
         pa.meta = reinterpret_cast<float2 *>(ws + w.meta);
         pa.O = O; pa.status = status_dev; pa.vec_out = dv % 4 == 0 ? 1 : 0;

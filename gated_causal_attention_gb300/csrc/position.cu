@@ -39,7 +39,7 @@ position_prep_kernel(PosArgs a, const __grid_constant__ HeadTable tab)
     const int slot = blockIdx.x, n = a.n;
     const float qk = tab.qk[slot];
     const float *av = a.a + (int64_t)(tab.bh[slot] % a.H) * n;
-    __nv_bfloat16 *kap = a.kap + (int64_t)slot * n;
+    __nv_bfloat16 *kap = a.kap + (int64_t)slot * a.kstride;
     float *C = a.C + (int64_t)slot * n;
     if (tid == 0) {
         s_bad = 0;
@@ -72,12 +72,11 @@ position_prep_kernel(PosArgs a, const __grid_constant__ HeadTable tab)
             flag_status(a.status, RS_STATUS_NONFINITE_BIT);
             a.meta[slot] = make_float2(0.f, __int_as_float(-1));
         }
-        for (int d = tid; d < n; d += kPrepThreads) {
-            kap[d] = __float2bfloat16_rn(0.f);
-            C[d] = 0.f;
-        }
+        for (int d = tid; d < a.kstride; d += kPrepThreads) kap[d] = __float2bfloat16_rn(0.f);
+        for (int d = tid; d < n; d += kPrepThreads) C[d] = 0.f;
         return;
     }
+    for (int d = n + tid; d < a.kstride; d += kPrepThreads) kap[d] = __float2bfloat16_rn(0.f);  // zero tail
     // kappa rounded to bf16, its inclusive prefix sum, the last nonzero offset
     for (int base = 0; base < n; base += kPrepThreads) {
         const int d = base + tid;
@@ -124,8 +123,7 @@ struct PosCfg {
     static constexpr int NSV = 4;                              // V stages
     static constexpr int NPB = 3;                              // P buffers in TMEM (64 columns each)
     static constexpr uint32_t ring = 0;
-    static constexpr uint32_t seg = ring + NSV * v_bytes;      // bf16 [NPB][256] kappa segments
-    static constexpr uint32_t rowf = seg + NPB * 512;          // float [128] row factors
+    static constexpr uint32_t rowf = ring + NSV * v_bytes;     // float [128] row factors
     static constexpr uint32_t bars = rowf + 512;               // vfull, vempty, pfull, pfree, accfull
     static constexpr int nbars = 2 * NSV + 2 * NPB + 1;
     static constexpr uint32_t misc = bars + nbars * 8;         // tmem slot, abort flag
@@ -225,48 +223,51 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
         }
     } else {
         // ------------------------------------------------------------ P builders
-        // Thread (h, r): row r of every P(delta), keys [64h, 64h + 64). The kappa segment of
-        // block offset delta, seg[e] = kappa(128 delta - 128 + e) (0 outside [0, n)), is staged
-        // by all 256 builders; key c of row r is seg[r - c + 128].
+        // Thread (h, r): row r of every P(delta), keys [64h, 64h + 64). With the kernel table
+        // read as 32-bit words, K32[w] = (kappa(2w), kappa(2w + 1)) (zero-padded past n), key c
+        // of row r in tile delta is kappa(128 delta + r - c). The 33 words a row needs are read
+        // through the read-only cache (the eight builder warps share them), a tile ahead.
         const int h = wg - 1, r = tid & 127, bt = tid - 128;  // bt: 0..255 over the builders
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const __nv_bfloat16 *kap = a.kap + (int64_t)slot * n;
+        const uint32_t *K32 = reinterpret_cast<const uint32_t *>(a.kap + (int64_t)slot * a.kstride);
+        // key pair (c, c+1), c = 64h + 2p: low half kappa(x), high half kappa(x - 1) with
+        // x = 128 delta + r - c; x - 1 = 128 delta - 128 + e0 for e0 = r - c + 127, whose parity
+        // is that of r + 1 for every pair of the row
+        const int e0top = r - 64 * h + 127;  // e0 of the first pair; each next pair is 2 lower
+        const bool odd = e0top & 1;
+        // words of tile t: index 64 t - 64 + ((e0top + 1) >> 1) - k, k = 0 .. 32 (odd rows use
+        // 33 words, even rows the first 32)
+        uint32_t wnext[33];
+        auto fetch = [&](int t, uint32_t (&w)[33]) {
+            const int w0 = 64 * t - 64 + ((e0top + 1) >> 1);
+#pragma unroll
+            for (int k = 0; k < 33; ++k) {
+                const int wi = w0 - k;
+                w[k] = wi >= 0 ? __ldg(K32 + wi) : 0u;  // negative offsets: 0 (causal)
+            }
+        };
+        if (T > 0) fetch(0, wnext);
         bool ok = true;
         for (int t = 0; t < T; ++t) {
             const int pb = t % NPB;
-            // buffer pb last held P(t - NPB): its MMA (and so every builder's reads of the
-            // segment, which came before the builders' arrivals) is done
-            if (ok && t >= NPB) ok = wait_bar_warp(pfree + pb, ((t / NPB) - 1) & 1, s_abort, a.status, 0);
-            unsigned short *seg = reinterpret_cast<unsigned short *>(smem + L::seg + pb * 512);
-            {
-                const int off = 128 * t - 128 + bt;
-                unsigned short v = 0;
-                if (off >= 0 && off < n) v = __bfloat16_as_ushort(kap[off]);
-                seg[bt] = v;
+            uint32_t wv[33];
+#pragma unroll
+            for (int k = 0; k < 33; ++k) wv[k] = wnext[k];
+            if (t + 1 < T) fetch(t + 1, wnext);
+            // buffer pb last held P(t - NPB): its MMA is done
+            if (t >= NPB && !wait_bar_warp(pfree + pb, ((t / NPB) - 1) & 1, s_abort, a.status, 0)) {
+                ok = false;
+                break;
             }
-            ok = named_bar_and(kBarBuild, 256, ok && !*s_abort);
-            if (!ok) break;
-            // key pair (c, c+1), c = 64h + 2p: low half seg[e0 + 1], high half seg[e0] with
-            // e0 = r - c + 127. Its parity is that of r + 1 for every pair of the row.
-            const uint32_t *seg32 = reinterpret_cast<const uint32_t *>(seg);
             uint32_t pk[32];
-            const int e0top = r - 64 * h + 127;  // e0 of the first pair; each next pair is 2 lower
-            if (e0top & 1) {
-                // e0 odd: the pair straddles words (e0 - 1)/2 (high half) and (e0 + 1)/2 (low half)
-                uint32_t wb = seg32[(e0top + 1) >> 1];
+            if (odd) {
+                // e0 odd: high half of word k+1 (kappa(x - 1)) with low half of word k (kappa(x))
 #pragma unroll
-                for (int p = 0; p < 32; ++p) {
-                    const uint32_t wa = seg32[((e0top - 2 * p) - 1) >> 1];
-                    pk[p] = __byte_perm(wb, wa, 0x7610);
-                    wb = wa;
-                }
+                for (int p = 0; p < 32; ++p) pk[p] = __byte_perm(wv[p], wv[p + 1], 0x7610);
             } else {
-                // e0 even: word e0/2 holds (seg[e0], seg[e0 + 1]); swap its halves
+                // e0 even: word k holds (kappa(x - 1), kappa(x)); swap its halves
 #pragma unroll
-                for (int p = 0; p < 32; ++p) {
-                    const uint32_t w = seg32[(e0top - 2 * p) >> 1];
-                    pk[p] = __byte_perm(w, 0u, 0x1032);
-                }
+                for (int p = 0; p < 32; ++p) pk[p] = __byte_perm(wv[p], 0u, 0x1032);
             }
             const uint32_t pc = trow + L::p_col0 + pb * 64 + 32 * h;
             RS_TMEM_ST16(pc, pk);
@@ -276,6 +277,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull + pb);
         }
+        ok = named_bar_and(kBarBuild, 256, ok && !*s_abort);
 
         // ------------------------------------------------------------ epilogue
         // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0

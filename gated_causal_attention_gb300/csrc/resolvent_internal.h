@@ -134,7 +134,8 @@ cudaError_t launch_operator(const OpArgs &a, const HeadTable &tab, const OpMaps 
 struct PosArgs {
     int n, H, dv;
     const float *a;              // [H, n] logit per offset d = i - j (head h of every batch reads row h)
-    __nv_bfloat16 *kap;          // [slots, n] kappa(d) = e^{qk a(d) - M} rounded to bf16 (scratch)
+    __nv_bfloat16 *kap;          // [slots, kstride] kappa(d) = e^{qk a(d) - M} rounded to bf16, 0 past n
+    int kstride;                 // kap row stride: ceil(n / 128) * 128 + 128
     float *C;                    // [slots, n] prefix sums of the rounded kappa (scratch)
     float2 *meta;                // [slots] (M, last offset whose kappa is not 0, as int bits)
     float *O;                    // [BH, n, dv]
