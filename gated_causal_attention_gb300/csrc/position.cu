@@ -121,23 +121,30 @@ template <int DVP>
 struct PosCfg {
     static constexpr uint32_t v_bytes = (DVP / 64) * kRegion;  // one V tile: 128 keys x DVP bf16
     static constexpr int NSV = 4;                              // V stages
-    static constexpr int NPB = 3;                              // P buffers in TMEM (64 columns each)
+    static constexpr int NPB = 4;                              // P buffers in TMEM (64 columns each)
     static constexpr uint32_t ring = 0;
-    static constexpr uint32_t rowf = ring + NSV * v_bytes;     // float [128] row factors
-    static constexpr uint32_t bars = rowf + 512;               // vfull, vempty, pfull, pfree, accfull
+    static constexpr uint32_t bars = ring + NSV * v_bytes;     // vfull, vempty, pfull, pfree, accfull
     static constexpr int nbars = 2 * NSV + 2 * NPB + 1;
     static constexpr uint32_t misc = bars + nbars * 8;         // tmem slot, abort flag
     static constexpr uint32_t end = misc + 16;
     static constexpr uint32_t alloc = end + 1024;
-    static constexpr uint32_t p_col0 = DVP;                    // TMEM: accumulator, then P buffers
-    static_assert(DVP + NPB * 64 <= 512, "TMEM budget");
-    static_assert((DVP / 32) * kRegion <= NSV * v_bytes, "epilogue staging in the V ring");
+    // TMEM: the accumulators of the lower and the upper query tile, then the P buffers
+    static constexpr uint32_t acc_hi = DVP, p_col0 = 2 * DVP;
+    static_assert(2 * DVP + NPB * 64 <= 512, "TMEM budget");
+    static_assert(2 * (DVP / 32) * kRegion <= NSV * v_bytes, "epilogue staging in the V ring");
     static_assert(alloc <= 227 * 1024, "shared memory");
 };
 
 constexpr int kPosThreads = 384;  // warpgroup 0: TMA (warp 0) and MMA (warp 1); 1-2: P builders
 constexpr int kBarBuild = 1;
 
+// One CTA takes two query tiles of one head, Qlo = 2m and Qhi = 2m + 1 (Qhi absent at the end
+// of an odd tile count). Step j loads V(Qhi - j) once and issues up to two MMAs with it:
+//   acc_hi += P(j) V(Qhi - j),  acc_lo += P(j - 1) V(Qlo - (j - 1)),
+// so P(delta), built once at step delta, serves the upper tile at step delta and the lower
+// tile at step delta + 1. Tile A (query tile Q_A, lag L_A: 0 for the upper tile, 1 for the
+// lower one when the upper exists) takes part at step j when 0 <= j - L_A <= D_A with
+// D_A = min(Q_A, the last block offset whose kernel is not all 0).
 template <int DVP>
 __global__ void __launch_bounds__(kPosThreads, 1)
 position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __grid_constant__ PosMaps maps)
@@ -152,24 +159,27 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
     uint64_t *vempty = vfull + NSV, *pfull = vfull + 2 * NSV, *pfree = pfull + NPB, *accfull = pfree + NPB;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L::misc) + 1;
-    float *s_rowf = reinterpret_cast<float *>(smem + L::rowf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
-    const int n = a.n, nqt = (n + 127) / 128;
+    const int n = a.n, nqt = (n + 127) / 128, npairs = (nqt + 1) / 2;
     // blocks run head group by head group (a group's V stays in L2 while its query tiles
-    // stream it), longest query tiles first within a group
+    // stream it), longest pairs first within a group
     const int G = a.heads_per_group;
-    const int grp = (int)blockIdx.x / (G * nqt);
-    const int rem = (int)blockIdx.x - grp * G * nqt;
+    const int grp = (int)blockIdx.x / (G * npairs);
+    const int rem = (int)blockIdx.x - grp * G * npairs;
     const int gsz = min(G, tab.count - grp * G);
-    const int QB = nqt - 1 - rem / gsz;
+    const int m = npairs - 1 - rem / gsz;
     const int slot = grp * G + rem % gsz;
     const int bh = tab.bh[slot];
     const float2 meta = a.meta[slot];  // (M, last offset whose kappa is not 0)
-    const int dmax = __float_as_int(meta.y);
-    // block offsets delta = 0 .. T-1 (key tile QB - delta); past the last nonzero kappa every
-    // entry of P(delta) is 0
-    const int T = min(QB, max((dmax + 127) / 128, 0)) + 1;
+    const int dmaxt = max((__float_as_int(meta.y) + 127) / 128, 0);  // last nonzero block offset
+    const int Qlo = 2 * m;
+    const bool has_hi = Qlo + 1 < nqt;
+    const int Qhi = has_hi ? Qlo + 1 : Qlo;
+    const int Dlo = min(Qlo, dmaxt), Dhi = has_hi ? min(Qhi, dmaxt) : -1;
+    const int Llo = has_hi ? 1 : 0;
+    const int S = max(Llo + Dlo, Dhi) + 1;  // steps
+    const int Dmax = max(Dlo, Dhi);         // P(0 .. Dmax) are built
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < L::nbars; ++i) mbar_init(vfull + i, 1);
@@ -189,34 +199,38 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
 
     if (wg == 0) {
         if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------------ TMA: V tiles
-            for (int t = 0; t < T; ++t) {
-                const int sv = t % NSV;
-                if (t >= NSV && !wait_bar(vempty + sv, ((t / NSV) - 1) & 1, s_abort, a.status, 256)) break;
+            // ------------------------------------------------------------ TMA: V(Qhi - j)
+            for (int j = 0; j < S; ++j) {
+                const int sv = j % NSV;
+                if (j >= NSV && !wait_bar(vempty + sv, ((j / NSV) - 1) & 1, s_abort, a.status, 256)) break;
                 unsigned char *stg = smem + L::ring + sv * L::v_bytes;
                 mbar_arrive_expect_tx(vfull + sv, L::v_bytes);
                 for (int rr = 0; rr < DVP / 64; ++rr)
-                    tma_load_3d(stg + rr * kRegion, &maps.v, vfull + sv, rr * 64, (QB - t) * 128, bh);
+                    tma_load_3d(stg + rr * kRegion, &maps.v, vfull + sv, rr * 64, (Qhi - j) * 128, bh);
             }
         } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA: O += P V
+            // ------------------------------------------------------------ MMA
             constexpr uint32_t idesc = idesc_bf16(128, DVP, false, true);
             const uint64_t dv0 = sw128_desc(sbase + L::ring, kRegion, 1024);
             bool ok = true;
-            for (int t = 0; t < T; ++t) {
-                const int pb = t % NPB, sv = t % NSV;
-                if (!wait_bar(pfull + pb, (t / NPB) & 1, s_abort, a.status, 32) ||
-                    !wait_bar(vfull + sv, (t / NSV) & 1, s_abort, a.status, 32)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t pcol = tmem + L::p_col0 + pb * 64;
-                const uint64_t dv = dv0 + (((uint32_t)sv * L::v_bytes) >> 4);
-                umma_bf16_ts(tmem, pcol, dv, idesc, t > 0 ? 1u : 0u);
+            auto pv = [&](uint32_t acc, int delta, uint64_t dv, uint32_t accumulate) {
+                const uint32_t pcol = tmem + L::p_col0 + (delta % NPB) * 64;
+                umma_bf16_ts(acc, pcol, dv, idesc, accumulate);
 #pragma unroll
-                for (int ks = 1; ks < 8; ++ks) umma_bf16_ts(tmem, pcol + ks * 8, dv + (ks * 2048 >> 4), idesc, 1u);
-                umma_commit(pfree + pb);
+                for (int ks = 1; ks < 8; ++ks) umma_bf16_ts(acc, pcol + ks * 8, dv + (ks * 2048 >> 4), idesc, 1u);
+            };
+            for (int j = 0; j < S; ++j) {
+                const int sv = j % NSV;
+                if (j <= Dmax && !wait_bar(pfull + j % NPB, (j / NPB) & 1, s_abort, a.status, 32)) ok = false;
+                if (ok && !wait_bar(vfull + sv, (j / NSV) & 1, s_abort, a.status, 32)) ok = false;
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dv = dv0 + (((uint32_t)sv * L::v_bytes) >> 4);
+                if (has_hi && j <= Dhi) pv(tmem + L::acc_hi, j, dv, j > 0 ? 1u : 0u);
+                const int dl = j - Llo;
+                if (dl >= 0 && dl <= Dlo) pv(tmem, dl, dv, dl > 0 ? 1u : 0u);
+                // P(j - 1) had its last use in this step (the upper tile took it at step j - 1)
+                if (j >= 1) umma_commit(pfree + (j - 1) % NPB);
                 umma_commit(vempty + sv);
             }
             if (ok) umma_commit(accfull);
@@ -246,15 +260,15 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
                 w[k] = wi >= 0 ? __ldg(K32 + wi) : 0u;  // negative offsets: 0 (causal)
             }
         };
-        if (T > 0) fetch(0, wnext);
+        fetch(0, wnext);
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t <= Dmax; ++t) {
             const int pb = t % NPB;
             uint32_t wv[33];
 #pragma unroll
             for (int k = 0; k < 33; ++k) wv[k] = wnext[k];
-            if (t + 1 < T) fetch(t + 1, wnext);
-            // buffer pb last held P(t - NPB): its MMA is done
+            if (t < Dmax) fetch(t + 1, wnext);
+            // buffer pb last held P(t - NPB): both of its MMAs are done
             if (t >= NPB && !wait_bar_warp(pfree + pb, ((t / NPB) - 1) & 1, s_abort, a.status, 0)) {
                 ok = false;
                 break;
@@ -277,15 +291,17 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull + pb);
         }
-        ok = named_bar_and(kBarBuild, 256, ok && !*s_abort);
 
         // ------------------------------------------------------------ epilogue
-        // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0
-        const int row = QB * 128 + r;
-        const bool valid = row < n;
-        if (h == 0) {
+        // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0.
+        // Thread (h, r) takes row r of the lower (h = 0) or the upper (h = 1) query tile.
+        const int QA = h ? Qhi : Qlo;
+        const bool mine = h == 0 || has_hi;
+        const int row = QA * 128 + r;
+        const bool valid = mine && row < n;
+        float f = 0.f;
+        {
             const float beta = tab.beta[slot], M = meta.x;
-            float f = 0.f;
             bool bad = false;
             if (valid) {
                 const float Ci = a.C[(int64_t)slot * n + row];
@@ -293,19 +309,19 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
                 f = (beta == 0.f) ? expf(M) : expf((1.f - beta) * M - beta * logf(Ci));
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
-            s_rowf[r] = f;
         }
         bool done = ok && wait_bar_warp(accfull, 0, s_abort, a.status, 0);
-        done = named_bar_and(kBarBuild, 256, done);  // also publishes the row factors
-        const float f = s_rowf[r];
-        constexpr int nq = DVP / 32;  // 32-column chunks; half h takes [h nq/2, (h+1) nq/2)
+        done = named_bar_and(kBarBuild, 256, done && !*s_abort);
+        constexpr int nq = DVP / 32;  // 32-column chunks of one accumulator row
         const uint32_t stage = sbase + L::ring;
-        if (done) {
+        if (done && mine) {
             tc_fence_after();
+            const uint32_t tacc = trow + (h ? L::acc_hi : 0u);
+            const uint32_t tstage = stage + h * nq * kRegion;
 #pragma unroll 1
-            for (int q = h * nq / 2; q < (h + 1) * nq / 2; ++q) {
+            for (int q = 0; q < nq; ++q) {
                 uint32_t acc[32];
-                RS_TMEM_LD32(trow + 32 * q, acc);  // warp-wide: every lane, valid row or not
+                RS_TMEM_LD32(tacc + 32 * q, acc);  // warp-wide: every lane, valid row or not
                 tmem_ld_wait();
                 if (a.vec_out) {
 #pragma unroll
@@ -316,7 +332,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
                             const float x = __uint_as_float(acc[4 * c + k]);
                             w[k] = __float_as_uint(x == 0.f ? 0.f : x * f);
                         }
-                        sts128(stage + q * kRegion + r * 128 + ((c ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+                        sts128(tstage + q * kRegion + r * 128 + ((c ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
                     }
                 } else if (valid) {  // rows of dv % 4 != 0 floats: plain stores from registers
                     float *o = a.O + ((int64_t)bh * n + row) * a.dv;
@@ -333,18 +349,23 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
         if (done && a.vec_out) {
             // coalesced 16-byte stores: lane l takes unit l % 8 of row l / 8 of four rows
             const int wi = bt >> 5, unit = lane & 7;
-            const int nrows = min(128, n - QB * 128);
-            float *o0 = a.O + ((int64_t)bh * n + QB * 128) * a.dv;
 #pragma unroll 1
-            for (int q = 0; q < nq; ++q) {
-                const int col = 32 * q + 4 * unit;
-                if (col >= a.dv) continue;
+            for (int tt = 0; tt < (has_hi ? 2 : 1); ++tt) {
+                const int Qt = tt ? Qhi : Qlo;
+                const int nrows = min(128, n - Qt * 128);
+                float *o0 = a.O + ((int64_t)bh * n + Qt * 128) * a.dv;
+                const uint32_t tstage = stage + tt * nq * kRegion;
+#pragma unroll 1
+                for (int q = 0; q < nq; ++q) {
+                    const int col = 32 * q + 4 * unit;
+                    if (col >= a.dv) continue;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rr = 32 * k + 4 * wi + (lane >> 3);
-                    if (rr >= nrows) continue;
-                    const uint4 v = lds128(stage + q * kRegion + rr * 128 + ((unit ^ (rr & 7)) << 4));
-                    *reinterpret_cast<uint4 *>(o0 + (int64_t)rr * a.dv + col) = v;
+                    for (int k = 0; k < 4; ++k) {
+                        const int rr = 32 * k + 4 * wi + (lane >> 3);
+                        if (rr >= nrows) continue;
+                        const uint4 v = lds128(tstage + q * kRegion + rr * 128 + ((unit ^ (rr & 7)) << 4));
+                        *reinterpret_cast<uint4 *>(o0 + (int64_t)rr * a.dv + col) = v;
+                    }
                 }
             }
         }
@@ -369,8 +390,8 @@ cudaError_t launch_pos(const PosArgs &a, const HeadTable &tab, const PosMaps &ma
     auto k = position_head_kernel<DVP>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
     if (e != cudaSuccess) return e;
-    const int nqt = (a.n + 127) / 128;
-    k<<<nqt * tab.count, kPosThreads, L::alloc, s>>>(a, tab, maps);
+    const int npairs = ((a.n + 127) / 128 + 1) / 2;
+    k<<<npairs * tab.count, kPosThreads, L::alloc, s>>>(a, tab, maps);
     return cudaGetLastError();
 }
 
