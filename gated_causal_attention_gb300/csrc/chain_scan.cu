@@ -115,7 +115,12 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     __shared__ int s_loaded;
     if (tid == 0) {
         s_loaded = !bulk || mbar_wait(&s_bar, 0, a.wait_limit_ns);
-        if (!s_loaded) flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
+        if (!s_loaded) {
+            flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
+            // the copy still lands in this CTA's shared memory: wait for it (with a limit of
+            // its own) before the CTA exits
+            mbar_wait(&s_bar, 0, 200000000ull);
+        }
     }
     __syncthreads();
     if (!s_loaded) return;  // the chunk never arrived: give up on it (uniform across the CTA)

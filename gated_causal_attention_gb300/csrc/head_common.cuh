@@ -47,6 +47,29 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, vo
     return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, status, sleep_ns));
 }
 
+// Winding down. Whatever a CTA started must end before it frees TMEM and exits: TMA copies
+// into its shared memory and tensor-core work on its TMEM and shared memory. After an abort
+// nothing else waits for them, so the roles that started them do, with a time limit of
+// their own that the abort flag does not cut short.
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
+
+// The TMA loads a producer issued into a ring of `nstages` stages with full barriers
+// full[0 .. nstages): `issued` loads in order, load t into stage t % nstages. Waits for the
+// phase of the last load of each stage (earlier phases of a barrier complete first).
+__device__ __forceinline__ void drain_loads(uint64_t *full, int nstages, int issued)
+{
+    for (int s = 0; s < nstages && s < issued; ++s)
+        mbar_wait(full + s, (uint32_t)((issued - 1 - s) / nstages) & 1u, kDrainLimitNs);
+}
+
+// Every tcgen05.mma this thread issued: a commit to `bar`, a barrier (count 1) that nothing
+// else uses, and a wait for its first phase.
+__device__ __forceinline__ void drain_mma(uint64_t *bar)
+{
+    umma_commit(bar);
+    mbar_wait(bar, 0, kDrainLimitNs);
+}
+
 __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32])
 {
     uint32_t r[32];

@@ -100,8 +100,8 @@ struct Cfg {
     static constexpr uint32_t upR = upA + 128 * 8;                    // float [128] prod |a_{64..i}|
     static constexpr uint32_t bars = upR + 128 * 4;                   // mbarriers
     // q; full, empty, vprep, rc (4 each); s_full, p_full, pv_done (3 each); vfull, vempty
-    // (4 each); diag_ready
-    static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4 + 1;
+    // (4 each); diag_ready; the two MMA issuers' drains
+    static constexpr int nbars = 1 + 4 * 4 + 3 * 3 + 2 * 4 + 1 + 2;
     static constexpr uint32_t misc = bars + nbars * 8;                // ints: tmem, -, abort, -, diag_all_live[4]
     static constexpr uint32_t end = misc + 64;
     static constexpr uint32_t alloc = end + 1024;
@@ -126,6 +126,7 @@ struct Barriers {
     // full/empty: the K+V ring (gated heads) or the K ring (g = 0); vfull/vempty: the V ring
     uint64_t *q, *full, *empty, *vprep, *rc, *s_full, *p_full, *pv_done, *vfull, *vempty;
     uint64_t *diag_ready;  // the value-prep warps have written the query block's gate data
+    uint64_t *drain_s, *drain_pv;  // each MMA issuer's own wait for its work when it winds down
 };
 
 template <int DP, int DVP, bool GATED>
@@ -142,7 +143,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bar0 = reinterpret_cast<uint64_t *>(smem + L::bars);
     Barriers B{bar0,      bar0 + 1,  bar0 + 5,  bar0 + 9,  bar0 + 13, bar0 + 17,
-               bar0 + 20, bar0 + 23, bar0 + 26, bar0 + 30, bar0 + 34};
+               bar0 + 20, bar0 + 23, bar0 + 26, bar0 + 30, bar0 + 34, bar0 + 35, bar0 + 36};
     int *misc = reinterpret_cast<int *>(smem + L::misc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 2;
@@ -218,6 +219,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && L::split) {  // the K ring
+            int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int st = t % L::NSK;
                 if (t >= L::NSK && !wait_bar(B.empty + st, ((t / L::NSK) - 1) & 1, s_abort, a.status, 256)) break;
@@ -226,8 +228,11 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 mbar_arrive_expect_tx(B.full + st, L::k_bytes);
                 for (int rr = 0; rr < DP / 64; ++rr)
                     tma_load_3d(stg + rr * kRegion, &maps.k, B.full + st, rr * 64, kb * 128, bh);
+                ++issued;
             }
+            drain_loads(B.full, L::NSK, issued);
         } else if (lane == 0) {
+            int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int st = t % NS;
                 if (t >= NS && !wait_bar(B.empty + st, ((t / NS) - 1) & 1, s_abort, a.status, 256)) break;
@@ -238,11 +243,15 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                     tma_load_3d(stg + rr * kRegion, &maps.k, B.full + st, rr * 64, kb * 128, bh);
                 for (int rr = 0; rr < DVP / 64; ++rr)
                     tma_load_3d(stg + L::k_bytes + rr * kRegion, &maps.v, B.full + st, rr * 64, kb * 128, bh);
+                ++issued;
             }
+            drain_loads(B.full, NS, issued);
         }
+        if (lane == 0) drain_loads(B.q, 1, 1);  // Q, loaded in the prologue
     } else if (L::split && warp == kTmaWarp + 3) {
         // ------------------------------------------------------------ TMA producer, V ring
         if (lane == 0) {
+            int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int sv = t % L::NSV;
                 if (t >= L::NSV && !wait_bar(B.vempty + sv, ((t / L::NSV) - 1) & 1, s_abort, a.status, 256)) break;
@@ -251,7 +260,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 mbar_arrive_expect_tx(B.vfull + sv, L::v_bytes);
                 for (int rr = 0; rr < DVP / 64; ++rr)
                     tma_load_3d(stg + rr * kRegion, &maps.v, B.vfull + sv, rr * 64, kb * 128, bh);
+                ++issued;
             }
+            drain_loads(B.vfull, L::NSV, issued);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer: S = Q K^T
@@ -283,6 +294,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 umma_commit(B.s_full + sb);
                 if (L::split) umma_commit(B.empty + st);  // the K stage is free once S is done
             }
+            drain_mma(B.drain_s);
         }
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------------ MMA issuer: O += P V'
@@ -322,6 +334,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 umma_commit(B.pv_done + sb);
                 umma_commit(L::split ? B.vempty + sv : B.empty + st);
             }
+            drain_mma(B.drain_pv);
         }
     }
     } else if (GATED && wg == RL::vprep_wg) {

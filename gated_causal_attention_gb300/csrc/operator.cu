@@ -75,8 +75,8 @@ struct OpLayout {
     static constexpr uint32_t rq = rows + 2 * 128 * 16;             // float [2][128]
     static constexpr uint32_t xchg = rq + 2 * 128 * 4;              // float4 [2][128] (stats)
     static constexpr uint32_t kind = xchg + 2 * 128 * 16;           // int [2], then float [2] cmin
-    static constexpr uint32_t bars = kind + 16;                     // kfull[2] sfull[2] sempty[2]
-    static constexpr uint32_t misc = bars + 6 * 8;                  // tmem slot, abort flag
+    static constexpr uint32_t bars = kind + 16;                     // kfull[2] sfull[2] sempty[2] drain
+    static constexpr uint32_t misc = bars + 7 * 8;                  // tmem slot, abort flag
     static constexpr uint32_t end = misc + 16;
     static constexpr uint32_t alloc = end + 1024;
     static_assert(alloc <= 227 * 1024, "shared memory");
@@ -94,6 +94,7 @@ struct OpSmem {
     volatile int *kind;
     volatile float *cmin;  // the smallest key-scale magnitude of the tile (off-diagonal tiles)
     uint64_t *kfull, *sfull, *sempty;
+    uint64_t *drain;  // the producer's own wait for its MMAs when it winds down
     uint32_t *tmem_slot;
     volatile int *abort;
 };
@@ -115,6 +116,7 @@ __device__ __forceinline__ OpSmem op_smem(unsigned char *smem_raw)
     m.kfull = reinterpret_cast<uint64_t *>(m.base + L::bars);
     m.sfull = m.kfull + 2;
     m.sempty = m.kfull + 4;
+    m.drain = m.kfull + 6;
     m.tmem_slot = reinterpret_cast<uint32_t *>(m.base + L::misc);
     m.abort = reinterpret_cast<volatile int *>(m.base + L::misc) + 1;
     return m;
@@ -135,6 +137,7 @@ __device__ __forceinline__ uint32_t op_setup(const OpSmem &m, const OpMaps &maps
             mbar_init(m.sfull + b, 2);  // the producer's release of the smem data + the MMA commit
             mbar_init(m.sempty + b, 8);
         }
+        mbar_init(m.drain, 1);
         *m.abort = 0;
         fence_mbar_init();
     }
@@ -152,8 +155,10 @@ __device__ __forceinline__ uint32_t op_setup(const OpSmem &m, const OpMaps &maps
     return *m.tmem_slot;
 }
 
-__device__ __forceinline__ void op_teardown(uint32_t tmem)
+__device__ __forceinline__ void op_teardown(const OpSmem &m, uint32_t tmem)
 {
+    // the producer lane issued every MMA of the CTA: they end before TMEM is freed
+    if ((threadIdx.x >> 5) == kProdWarp && (threadIdx.x & 31) == 0) drain_mma(m.drain);
     tc_fence_before();
     __syncthreads();
     if ((threadIdx.x >> 5) == 0) {
@@ -234,6 +239,9 @@ __device__ __forceinline__ bool produce_tile(const OpArgs &a, const OpMaps &maps
             mbar_arrive(m.sfull + b);
         } else {
             ok = wait_bar(m.kfull + b, (kph >> b) & 1u, m.abort, a.status);
+            // the loads of this tile are the only ones in flight: after a timeout they still
+            // land before the CTA exits
+            if (!ok) mbar_wait(m.kfull + b, (kph >> b) & 1u, kDrainLimitNs);
             if (ok) {
                 tc_fence_after();
                 constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
@@ -475,7 +483,7 @@ operator_stats_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __g
             }
         }
     }
-    op_teardown(tmem);
+    op_teardown(m, tmem);
 }
 
 // ================================================================ row data
@@ -732,7 +740,7 @@ operator_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __grid_co
         if (TMA_OUT && lane == 0) bulk_wait_all();
         __syncwarp();
     }
-    op_teardown(tmem);
+    op_teardown(m, tmem);
 }
 
 template <int DP, bool GATED>

@@ -123,8 +123,8 @@ struct PosCfg {
     static constexpr int NSV = 4;                              // V stages
     static constexpr int NPB = 4;                              // P buffers in TMEM (64 columns each)
     static constexpr uint32_t ring = 0;
-    static constexpr uint32_t bars = ring + NSV * v_bytes;     // vfull, vempty, pfull, pfree, accfull
-    static constexpr int nbars = 2 * NSV + 2 * NPB + 1;
+    static constexpr uint32_t bars = ring + NSV * v_bytes;     // vfull, vempty, pfull, pfree, accfull, drain
+    static constexpr int nbars = 2 * NSV + 2 * NPB + 2;
     static constexpr uint32_t misc = bars + nbars * 8;         // tmem slot, abort flag
     static constexpr uint32_t end = misc + 16;
     static constexpr uint32_t alloc = end + 1024;
@@ -157,6 +157,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
     const uint32_t sbase = smem_u32(smem);
     uint64_t *vfull = reinterpret_cast<uint64_t *>(smem + L::bars);
     uint64_t *vempty = vfull + NSV, *pfull = vfull + 2 * NSV, *pfree = pfull + NPB, *accfull = pfree + NPB;
+    uint64_t *drain = accfull + 1;  // the MMA issuer's own wait for its work when it winds down
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L::misc) + 1;
 
@@ -200,6 +201,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
     if (wg == 0) {
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------------ TMA: V(Qhi - j)
+            int issued = 0;
             for (int j = 0; j < S; ++j) {
                 const int sv = j % NSV;
                 if (j >= NSV && !wait_bar(vempty + sv, ((j / NSV) - 1) & 1, s_abort, a.status, 256)) break;
@@ -207,7 +209,9 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
                 mbar_arrive_expect_tx(vfull + sv, L::v_bytes);
                 for (int rr = 0; rr < DVP / 64; ++rr)
                     tma_load_3d(stg + rr * kRegion, &maps.v, vfull + sv, rr * 64, (Qhi - j) * 128, bh);
+                ++issued;
             }
+            drain_loads(vfull, NSV, issued);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------ MMA
             constexpr uint32_t idesc = idesc_bf16(128, DVP, false, true);
@@ -234,6 +238,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
                 umma_commit(vempty + sv);
             }
             if (ok) umma_commit(accfull);
+            drain_mma(drain);
         }
     } else {
         // ------------------------------------------------------------ P builders
