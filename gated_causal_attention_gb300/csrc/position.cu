@@ -120,18 +120,21 @@ position_prep_kernel(PosArgs a, const __grid_constant__ HeadTable tab)
 template <int DVP>
 struct PosCfg {
     static constexpr uint32_t v_bytes = (DVP / 64) * kRegion;  // one V tile: 128 keys x DVP bf16
-    static constexpr int NSV = 4;                              // V stages
-    static constexpr int NPB = 4;                              // P buffers in TMEM (64 columns each)
-    static constexpr uint32_t ring = 0;
-    static constexpr uint32_t bars = ring + NSV * v_bytes;     // vfull, vempty, pfull, pfree, accfull, drain
+    static constexpr int NSV = 3;                              // V stages
+    static constexpr int NPB = 4;                              // P blocks
+    // P block b, keys [64 kr, 64 kr + 64) of its 128 rows: p_ring + kr * p_half + b * kRegion,
+    // so the rows of consecutive blocks b, b + 1 follow one another in each key half
+    static constexpr uint32_t p_half = NPB * kRegion;
+    static constexpr uint32_t v_ring = 0;
+    static constexpr uint32_t p_ring = v_ring + NSV * v_bytes;
+    static constexpr uint32_t rowf = p_ring + 2 * p_half;      // float [2][128] row factors
+    static constexpr uint32_t bars = rowf + 2 * 128 * 4;       // vfull, vempty, pfull, pfree, accfull, drain
     static constexpr int nbars = 2 * NSV + 2 * NPB + 2;
     static constexpr uint32_t misc = bars + nbars * 8;         // tmem slot, abort flag
     static constexpr uint32_t end = misc + 16;
     static constexpr uint32_t alloc = end + 1024;
-    // TMEM: the accumulators of the lower and the upper query tile, then the P buffers
-    static constexpr uint32_t acc_hi = DVP, p_col0 = 2 * DVP;
-    static_assert(2 * DVP + NPB * 64 <= 512, "TMEM budget");
-    static_assert(2 * (DVP / 32) * kRegion <= NSV * v_bytes, "epilogue staging in the V ring");
+    // the epilogue stages both output tiles (fp32, [query][dv]) over the V and P rings
+    static_assert(2 * 128 * DVP * 4 <= rowf, "epilogue staging");
     static_assert(alloc <= 227 * 1024, "shared memory");
 };
 
@@ -139,11 +142,15 @@ constexpr int kPosThreads = 384;  // warpgroup 0: TMA (warp 0) and MMA (warp 1);
 constexpr int kBarBuild = 1;
 
 // One CTA takes two query tiles of one head, Qlo = 2m and Qhi = 2m + 1 (Qhi absent at the end
-// of an odd tile count). Step j loads V(Qhi - j) once and issues up to two MMAs with it:
-//   acc_hi += P(j) V(Qhi - j),  acc_lo += P(j - 1) V(Qlo - (j - 1)),
-// so P(delta), built once at step delta, serves the upper tile at step delta and the lower
-// tile at step delta + 1. Tile A (query tile Q_A, lag L_A: 0 for the upper tile, 1 for the
-// lower one when the upper exists) takes part at step j when 0 <= j - L_A <= D_A with
+// of an odd tile count), and computes their outputs transposed, O^T = V^T P^T, so that the
+// tensor core reads V (the A operand) once for both tiles: accumulator lane = value
+// column, TMEM column = query (the lower tile's 128, then the upper tile's).
+// Step j loads V(Qhi - j); the upper tile takes it with P(j) and the lower one with P(j - 1).
+// Both are blocks of one causal Toeplitz matrix (entry kappa(query - key)): the upper tile's
+// rows of step j - 1 are the lower tile's rows of step j, so each P block is built once, and
+// when P(j - 1) and P(j) sit in consecutive buffers one N = 256 MMA covers both tiles.
+// Tile A (query tile Q_A, lag L_A: 0 for the upper tile, 1 for the lower one when the upper
+// exists) takes part at step j when 0 <= j - L_A <= D_A with
 // D_A = min(Q_A, the last block offset whose kernel is not all 0).
 template <int DVP>
 __global__ void __launch_bounds__(kPosThreads, 1)
@@ -160,6 +167,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
     uint64_t *drain = accfull + 1;  // the MMA issuer's own wait for its work when it winds down
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L::misc) + 1;
+    float *s_rowf = reinterpret_cast<float *>(smem + L::rowf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
     const int n = a.n, nqt = (n + 127) / 128, npairs = (nqt + 1) / 2;
@@ -190,7 +198,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
         prefetch_tmap(&maps.v);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 512);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -205,7 +213,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
             for (int j = 0; j < S; ++j) {
                 const int sv = j % NSV;
                 if (j >= NSV && !wait_bar(vempty + sv, ((j / NSV) - 1) & 1, s_abort, a.status, 256)) break;
-                unsigned char *stg = smem + L::ring + sv * L::v_bytes;
+                unsigned char *stg = smem + L::v_ring + sv * L::v_bytes;
                 mbar_arrive_expect_tx(vfull + sv, L::v_bytes);
                 for (int rr = 0; rr < DVP / 64; ++rr)
                     tma_load_3d(stg + rr * kRegion, &maps.v, vfull + sv, rr * 64, (Qhi - j) * 128, bh);
@@ -213,48 +221,68 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
             }
             drain_loads(vfull, NSV, issued);
         } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA
-            constexpr uint32_t idesc = idesc_bf16(128, DVP, false, true);
-            const uint64_t dv0 = sw128_desc(sbase + L::ring, kRegion, 1024);
-            bool ok = true;
-            auto pv = [&](uint32_t acc, int delta, uint64_t dv, uint32_t accumulate) {
-                const uint32_t pcol = tmem + L::p_col0 + (delta % NPB) * 64;
-                umma_bf16_ts(acc, pcol, dv, idesc, accumulate);
-#pragma unroll
-                for (int ks = 1; ks < 8; ++ks) umma_bf16_ts(acc, pcol + ks * 8, dv + (ks * 2048 >> 4), idesc, 1u);
+            // ------------------------------------------------------------ MMA: O^T += V^T P^T
+            constexpr uint32_t idesc1 = idesc_bf16(128, 128, true, false);  // one tile
+            constexpr uint32_t idesc2 = idesc_bf16(128, 256, true, false);  // both tiles
+            // V^T: value columns contiguous (64 per 128-byte row, 16 KB to the next 64; for
+            // DVP = 64 the upper half of M reads the next buffer and lands in unused lanes)
+            const uint64_t da0 = sw128_desc(sbase + L::v_ring, kRegion, 1024);
+            // P^T: keys contiguous, 128-byte swizzled rows; the K-step offset is added later
+            const uint64_t dp0 = sw128_desc(sbase + L::p_ring, 16, 1024);
+            auto dp = [&](int b, int ks) {
+                return dp0 + (((uint32_t)(ks >> 2) * L::p_half + (uint32_t)b * kRegion + (uint32_t)(ks & 3) * 32) >> 4);
             };
+            bool ok = true;
             for (int j = 0; j < S; ++j) {
                 const int sv = j % NSV;
-                if (j <= Dmax && !wait_bar(pfull + j % NPB, (j / NPB) & 1, s_abort, a.status, 32)) ok = false;
-                if (ok && !wait_bar(vfull + sv, (j / NSV) & 1, s_abort, a.status, 32)) ok = false;
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t dv = dv0 + (((uint32_t)sv * L::v_bytes) >> 4);
-                if (has_hi && j <= Dhi) pv(tmem + L::acc_hi, j, dv, j > 0 ? 1u : 0u);
                 const int dl = j - Llo;
-                if (dl >= 0 && dl <= Dlo) pv(tmem, dl, dv, dl > 0 ? 1u : 0u);
-                // P(j - 1) had its last use in this step (the upper tile took it at step j - 1)
-                if (j >= 1) umma_commit(pfree + (j - 1) % NPB);
+                const bool lo = dl >= 0 && dl <= Dlo, hi = has_hi && j <= Dhi;
+                // P(j) is new at this step (P(dl) of the lower tile was waited for at step dl)
+                if (!wait_bar(vfull + sv, (j / NSV) & 1, s_abort, a.status, 32) ||
+                    ((hi || (lo && Llo == 0)) && !wait_bar(pfull + j % NPB, (j / NPB) & 1, s_abort, a.status, 32))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t da = da0 + (((uint32_t)sv * L::v_bytes) >> 4);
+                const int blo = (dl >= 0 ? dl : 0) % NPB;
+                if (lo && hi && dl >= 1 && blo + 1 < NPB) {
+                    // P(j - 1), P(j) in consecutive buffers: 256 consecutive query rows
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) umma_bf16_ss(tmem, da + (ks * 2048 >> 4), dp(blo, ks), idesc2, 1u);
+                } else {
+                    if (lo) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            umma_bf16_ss(tmem, da + (ks * 2048 >> 4), dp(blo, ks), idesc1, (dl > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    if (hi) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            umma_bf16_ss(tmem + 128, da + (ks * 2048 >> 4), dp(j % NPB, ks), idesc1, (j > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
                 umma_commit(vempty + sv);
+                if (lo) umma_commit(pfree + blo);  // the last use of P(dl)
             }
             if (ok) umma_commit(accfull);
             drain_mma(drain);
         }
     } else {
         // ------------------------------------------------------------ P builders
-        // Thread (h, r): row r of every P(delta), keys [64h, 64h + 64). With the kernel table
-        // read as 32-bit words, K32[w] = (kappa(2w), kappa(2w + 1)) (zero-padded past n), key c
-        // of row r in tile delta is kappa(128 delta + r - c). The 33 words a row needs are read
-        // through the read-only cache (the eight builder warps share them), a tile ahead.
+        // Thread (h, r): row r of every P(delta), keys [64h, 64h + 64): one 128-byte swizzled
+        // row of key half h. With the kernel table read as 32-bit words, K32[w] =
+        // (kappa(2w), kappa(2w + 1)) (zero-padded past n), key c of row r in block delta is
+        // kappa(128 delta + r - c). The 33 words a row needs are read through the read-only
+        // cache (the eight builder warps share them), a block ahead.
         const int h = wg - 1, r = tid & 127, bt = tid - 128;  // bt: 0..255 over the builders
-        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t *K32 = reinterpret_cast<const uint32_t *>(a.kap + (int64_t)slot * a.kstride);
         // key pair (c, c+1), c = 64h + 2p: low half kappa(x), high half kappa(x - 1) with
         // x = 128 delta + r - c; x - 1 = 128 delta - 128 + e0 for e0 = r - c + 127, whose parity
         // is that of r + 1 for every pair of the row
         const int e0top = r - 64 * h + 127;  // e0 of the first pair; each next pair is 2 lower
         const bool odd = e0top & 1;
-        // words of tile t: index 64 t - 64 + ((e0top + 1) >> 1) - k, k = 0 .. 32 (odd rows use
+        // words of block t: index 64 t - 64 + ((e0top + 1) >> 1) - k, k = 0 .. 32 (odd rows use
         // 33 words, even rows the first 32)
         uint32_t wnext[33];
         auto fetch = [&](int t, uint32_t (&w)[33]) {
@@ -266,6 +294,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
             }
         };
         fetch(0, wnext);
+        const uint32_t prow = sbase + L::p_ring + h * L::p_half + r * 128;
         bool ok = true;
         for (int t = 0; t <= Dmax; ++t) {
             const int pb = t % NPB;
@@ -273,7 +302,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
 #pragma unroll
             for (int k = 0; k < 33; ++k) wv[k] = wnext[k];
             if (t < Dmax) fetch(t + 1, wnext);
-            // buffer pb last held P(t - NPB): both of its MMAs are done
+            // buffer pb last held P(t - NPB): the MMAs that read it are done
             if (t >= NPB && !wait_bar_warp(pfree + pb, ((t / NPB) - 1) & 1, s_abort, a.status, 0)) {
                 ok = false;
                 break;
@@ -288,89 +317,81 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
 #pragma unroll
                 for (int p = 0; p < 32; ++p) pk[p] = __byte_perm(wv[p], 0u, 0x1032);
             }
-            const uint32_t pc = trow + L::p_col0 + pb * 64 + 32 * h;
-            RS_TMEM_ST16(pc, pk);
-            RS_TMEM_ST16(pc + 16, (pk + 16));
-            tmem_st_wait();
-            tc_fence_before();
+            const uint32_t dst = prow + pb * kRegion;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                sts128(dst + ((c ^ (r & 7)) << 4), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+            fence_proxy_async_smem();  // the tensor core reads P through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull + pb);
         }
 
         // ------------------------------------------------------------ epilogue
         // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0.
-        // Thread (h, r) takes row r of the lower (h = 0) or the upper (h = 1) query tile.
-        const int QA = h ? Qhi : Qlo;
-        const bool mine = h == 0 || has_hi;
-        const int row = QA * 128 + r;
-        const bool valid = mine && row < n;
-        float f = 0.f;
+        // Thread (h, r) works out the factor of row r of the lower (h = 0) or upper (h = 1) tile.
         {
-            const float beta = tab.beta[slot], M = meta.x;
+            const int QA = h ? Qhi : Qlo;
+            const int row = QA * 128 + r;
+            float f = 0.f;
             bool bad = false;
-            if (valid) {
+            if ((h == 0 || has_hi) && row < n) {
+                const float beta = tab.beta[slot], M = meta.x;
                 const float Ci = a.C[(int64_t)slot * n + row];
                 bad = !(Ci > 0.f);  // every kappa of the row underflowed
                 f = (beta == 0.f) ? expf(M) : expf((1.f - beta) * M - beta * logf(Ci));
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
+            s_rowf[h * 128 + r] = f;
         }
         bool done = ok && wait_bar_warp(accfull, 0, s_abort, a.status, 0);
+        // every MMA is done: the rings are free for staging; also publishes the row factors
         done = named_bar_and(kBarBuild, 256, done && !*s_abort);
-        constexpr int nq = DVP / 32;  // 32-column chunks of one accumulator row
-        const uint32_t stage = sbase + L::ring;
-        if (done && mine) {
+        // Warpgroup h moves tile h out of TMEM, times its row factors: lane d (value column) of
+        // TMEM columns [128 h, 128 h + 128), into a [query][DVP] fp32 block, 32 queries at a time
+        float *stage = reinterpret_cast<float *>(smem + L::v_ring);
+        const int d = (warp & 3) * 32 + lane;
+        if (done && (h == 0 || has_hi)) {
             tc_fence_after();
-            const uint32_t tacc = trow + (h ? L::acc_hi : 0u);
-            const uint32_t tstage = stage + h * nq * kRegion;
+            const uint32_t tcol = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 128 * h;
+            float *st = stage + h * 128 * DVP;
+            const float *rf = s_rowf + h * 128;
 #pragma unroll 1
-            for (int q = 0; q < nq; ++q) {
+            for (int qc = 0; qc < 4; ++qc) {
                 uint32_t acc[32];
-                RS_TMEM_LD32(tacc + 32 * q, acc);  // warp-wide: every lane, valid row or not
+                RS_TMEM_LD32(tcol + 32 * qc, acc);  // warp-wide
                 tmem_ld_wait();
-                if (a.vec_out) {
+                if (d < DVP) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float x = __uint_as_float(acc[4 * c + k]);
-                            w[k] = __float_as_uint(x == 0.f ? 0.f : x * f);
-                        }
-                        sts128(tstage + q * kRegion + r * 128 + ((c ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+                    for (int e = 0; e < 32; ++e) {
+                        const float x = __uint_as_float(acc[e]);
+                        st[(32 * qc + e) * DVP + d] = x == 0.f ? 0.f : x * rf[32 * qc + e];
                     }
-                } else if (valid) {  // rows of dv % 4 != 0 floats: plain stores from registers
-                    float *o = a.O + ((int64_t)bh * n + row) * a.dv;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * q + e < a.dv) {
-                            const float x = __uint_as_float(acc[e]);
-                            o[32 * q + e] = x == 0.f ? 0.f : x * f;
-                        }
                 }
             }
         }
         done = named_bar_and(kBarBuild, 256, done);
-        if (done && a.vec_out) {
-            // coalesced 16-byte stores: lane l takes unit l % 8 of row l / 8 of four rows
-            const int wi = bt >> 5, unit = lane & 7;
+        if (done) {
+            // coalesced stores: warp wi of the eight copies rows wi, wi + 8, ..., 16 bytes a lane
+            const int wi = bt >> 5;
 #pragma unroll 1
             for (int tt = 0; tt < (has_hi ? 2 : 1); ++tt) {
                 const int Qt = tt ? Qhi : Qlo;
                 const int nrows = min(128, n - Qt * 128);
                 float *o0 = a.O + ((int64_t)bh * n + Qt * 128) * a.dv;
-                const uint32_t tstage = stage + tt * nq * kRegion;
+                const float *st = stage + tt * 128 * DVP;
+                if (a.vec_out) {
 #pragma unroll 1
-                for (int q = 0; q < nq; ++q) {
-                    const int col = 32 * q + 4 * unit;
-                    if (col >= a.dv) continue;
+                    for (int q = wi; q < nrows; q += 8) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int rr = 32 * k + 4 * wi + (lane >> 3);
-                        if (rr >= nrows) continue;
-                        const uint4 v = lds128(tstage + q * kRegion + rr * 128 + ((unit ^ (rr & 7)) << 4));
-                        *reinterpret_cast<uint4 *>(o0 + (int64_t)rr * a.dv + col) = v;
+                        for (int c = 4 * lane; c < DVP; c += 128)
+                            if (c < a.dv)
+                                *reinterpret_cast<float4 *>(o0 + (int64_t)q * a.dv + c) =
+                                    *reinterpret_cast<const float4 *>(st + q * DVP + c);
                     }
+                } else {  // rows of dv % 4 != 0 floats: one value per store
+#pragma unroll 1
+                    for (int q = wi; q < nrows; q += 8)
+                        for (int c = lane; c < a.dv; c += 32) o0[(int64_t)q * a.dv + c] = st[q * DVP + c];
                 }
             }
         }
@@ -381,7 +402,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 256);
     }
 }
 
