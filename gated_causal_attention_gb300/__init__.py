@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.resolvent_test_set_wait_limit_ns.restype = None
         L.resolvent_test_set_chain_withhold.argtypes = [_I]
         L.resolvent_test_set_chain_withhold.restype = None
+        L.resolvent_test_set_position_withhold.argtypes = [_I]
+        L.resolvent_test_set_position_withhold.restype = None
         L.resolvent_profile_enable.argtypes = [_I]
         L.resolvent_profile_enable.restype = _I
         L.resolvent_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_float), _I]
@@ -365,6 +367,10 @@ def test_set_wait_limit_ns(ns: int) -> None:
 
 def test_set_chain_withhold(ticket: int) -> None:
     lib().resolvent_test_set_chain_withhold(int(ticket))
+
+
+def test_set_position_withhold(block: int) -> None:
+    lib().resolvent_test_set_position_withhold(int(block))
 
 
 def profile_enable(on: bool = True) -> None:

@@ -19,6 +19,7 @@ namespace {
 thread_local int g_launches = 0;
 uint64_t g_wait_limit_ns = kWaitLimitNs;
 int g_chain_withhold = -1;
+int g_position_withhold = -1;
 
 // Optional timing of the main kernel of each call (the fused head, or the chain scan when
 // a call has no other heads): a ring of CUDA event pairs recorded on the caller's stream.
@@ -583,6 +584,7 @@ rs_status resolvent_position_head(const float *a, const void *v, rs_switches sw,
         pa.C = reinterpret_cast<float *>(ws + w.C);
         pa.meta = reinterpret_cast<float2 *>(ws + w.meta);
         pa.O = O; pa.status = status_dev; pa.vec_out = dv % 4 == 0 ? 1 : 0;
+        pa.withhold = g_position_withhold;
         // about 24 MB of V per head group: a group's V tiles stay in L2
         const size_t v_head = (size_t)n * DVP * 2;
         pa.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / v_head));
@@ -723,6 +725,7 @@ rs_status resolvent_debug_path_product(const float *u, const float *theta, rs_sw
 // (so the bounded wait can be seen to run out without a hang).
 void resolvent_test_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kWaitLimitNs; }
 void resolvent_test_set_chain_withhold(int ticket) { g_chain_withhold = ticket; }
+void resolvent_test_set_position_withhold(int block) { g_position_withhold = block; }
 
 rs_status resolvent_profile_enable(int on)
 {

@@ -212,6 +212,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
             int issued = 0;
             for (int j = 0; j < S; ++j) {
                 const int sv = j % NSV;
+                if (j == 1 && (int)blockIdx.x == a.withhold) break;  // test knob (timeout path)
                 if (j >= NSV && !wait_bar(vempty + sv, ((j / NSV) - 1) & 1, s_abort, a.status, 256)) break;
                 unsigned char *stg = smem + L::v_ring + sv * L::v_bytes;
                 mbar_arrive_expect_tx(vfull + sv, L::v_bytes);

@@ -142,6 +142,7 @@ struct PosArgs {
     int32_t *status;
     int vec_out;                 // O staged and written by 16-byte stores (dv % 4 == 0)
     int heads_per_group;         // blocks are ordered head group by head group
+    int withhold;                // test knob: this block's V loads stop after its first (-1: none)
 };
 // v (bf16, box 64 x 128).
 struct PosMaps {

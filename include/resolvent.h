@@ -248,10 +248,15 @@ rs_status resolvent_debug_path_product(const float *u, const float *theta, rs_sw
  * Test knobs (tests only; they change how later calls on any thread behave):
  *  - the bound on device-side waits in the chain scan, in nanoseconds (0 restores 2 s);
  *  - a chain chunk ticket that never publishes its carry (-1: none), so that the bounded
- *    wait of the chunks after it runs out and RS_STATUS_TIMEOUT is raised without a hang.
+ *    wait of the chunks after it runs out and RS_STATUS_TIMEOUT is raised without a hang;
+ *  - a block of the position-head kernel whose V loads stop after its first (-1: none): its
+ *    tensor-core issuer's wait for the next V tile runs out (2 s), RS_STATUS_TIMEOUT is
+ *    raised, every block winds down (each waits for the copies and products it started) and
+ *    the call returns.
  */
 void resolvent_test_set_wait_limit_ns(uint64_t ns);
 void resolvent_test_set_chain_withhold(int ticket);
+void resolvent_test_set_position_withhold(int block);
 
 /*
  * Kernel timing (benchmarking): while enabled, each call records a pair of CUDA events on

@@ -511,6 +511,28 @@ def test_position_head_rows_sum_to_one_and_causal(R):
     assert not torch.equal(O1[:, :, 333:], O2[:, :, 333:])
 
 
+def test_position_bounded_wait_reports_timeout(R, oracle_mod):
+    """A block whose V loads stop after its first makes its tensor-core issuer's bounded wait
+    run out (2 s): the status word says so, every block winds down (waiting for the copies
+    and products it started) and the call returns; the next call is correct."""
+    B, H, n, dv = 1, 2, 1024, 64
+    pi = W.position_inputs(B, H, n, dv, seed=43, slope_scale=0.01)
+    a, v = dev(pi.a), dev(pi.v.reshape(B, H, n, dv), torch.bfloat16)
+    R.test_set_position_withhold(0)  # block 0 takes the longest pair: at least two steps
+    try:
+        with pytest.raises(R.DeviceTimeout):
+            R.position_head(a, v, 1.0, 1.0)
+    finally:
+        R.test_set_position_withhold(-1)
+    O = R.position_head(a, v, 1.0, 1.0)  # the context is still usable
+    torch.cuda.synchronize()
+    bq, qq = [f32(x) for x in pi.switches_bh()]
+    ref, st = oracle_mod.position_heads(pi.a, pi.v, bq, qq)
+    absr, _ = oracle_mod.position_heads(pi.a, np.abs(pi.v), bq, qq)
+    err = np.abs(O.cpu().double().numpy().reshape(B * H, n, dv) - ref)
+    assert np.all(err <= 2.0 ** -7 * absr + 1e-6 * (1.0 + np.max(absr)))
+
+
 def test_position_head_refusals(R):
     """Non-finite a (even at qk = 0) and a row whose kernel all underflows are refused; a gate
     switch other than 0 is not this form."""
