@@ -86,6 +86,9 @@ def lib():
             L.ro_position_heads.argtypes = [_f32p, _f32p, _i64, _i64, _i64, _i64, _f64p, _f64p,
                                             _f64p, _i32p, ctypes.c_int]
             L.ro_position_heads.restype = ctypes.c_int
+            L.ro_position_rows.argtypes = [_f32p, _f32p, _i64, _i64, _f64, _f64, _i64p, _i64,
+                                           _f64p]
+            L.ro_position_rows.restype = ctypes.c_int
             L.ro_max_threads.argtypes = []
             L.ro_max_threads.restype = ctypes.c_int
             _lib = L
@@ -275,6 +278,21 @@ def position_head(a, v, beta: float, qk: float) -> np.ndarray:
         raise ShapeError()
     O = np.zeros((n, va.shape[1]))
     _raise(lib().ro_position_head(pa, pv, n, va.shape[1], float(beta), float(qk), _ptr64(O)))
+    return O
+
+
+def position_rows(a, v, beta: float, qk: float, rows) -> np.ndarray:
+    """Rows `rows` of one position-only head (same arithmetic as position_head): a [n],
+    v [n,dv]; returns O [len(rows), dv]."""
+    aa, pa = _f32(a)
+    va, pv = _f32(v)
+    n = aa.size
+    if va.ndim != 2 or va.shape[0] != n:
+        raise ShapeError()
+    rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    O = np.zeros((rr.size, va.shape[1]))
+    _raise(lib().ro_position_rows(pa, pv, n, va.shape[1], float(beta), float(qk),
+                                  rr.ctypes.data_as(_i64p), rr.size, _ptr64(O)))
     return O
 
 

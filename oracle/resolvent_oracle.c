@@ -406,36 +406,76 @@ int ro_chain_heads(const float *u, const float *theta, const double *g, const fl
 }
 
 /* Position-only head: the definition row by row (see the header). */
+/* Row i of a position-only head from the logits t[d] = qk a(d) of every offset: a softmax
+ * row of t[i - j], j <= i, with Z_i taken from the sum shifted by the row maximum (every
+ * entry is live), O_i = sum_j e^{t[i-j]} v_j / Z_i^beta. */
+static void position_row(const double *t, const float *v, int64_t i, int64_t dv, double beta,
+                         double *Orow)
+{
+    double M = -INFINITY;
+    for (int64_t j = 0; j <= i; ++j)
+        if (t[i - j] > M) M = t[i - j];
+    double Zs = 0.0;
+    for (int64_t j = 0; j <= i; ++j) Zs += exp(t[i - j] - M);
+    const double logZ = M + log(Zs);
+    for (int64_t c = 0; c < dv; ++c) Orow[c] = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+        const double w = exp(t[i - j] - (beta == 0.0 ? 0.0 : beta * logZ));
+        for (int64_t c = 0; c < dv; ++c) Orow[c] += w * (double)v[j * dv + c];
+    }
+}
+
+/* The logits of every offset, refusing a non-finite a(d) (even at qk = 0) or qk a(d);
+ * NULL after a refusal (*rc set) or when out of memory. */
+static double *position_logits(const float *a, int64_t n, double qk, int *rc)
+{
+    *rc = RO_OK;
+    if (!all_finite(a, n)) {
+        *rc = RO_NONFINITE;
+        return NULL;
+    }
+    double *t = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!t) {
+        *rc = RO_SHAPE;
+        return NULL;
+    }
+    for (int64_t d = 0; d < n; ++d) {
+        t[d] = qk * (double)a[d];  /* the logit of every pair at offset d */
+        if (!isfinite(t[d])) {
+            free(t);
+            *rc = RO_NONFINITE;
+            return NULL;
+        }
+    }
+    return t;
+}
+
 int ro_position_head(const float *a, const float *v, int64_t n, int64_t dv, double beta,
                      double qk, double *O)
 {
     if (n == 0) return RO_OK;
     if (n < 0 || dv <= 0) return RO_SHAPE;
     if (!isfinite(beta) || !isfinite(qk)) return RO_NONFINITE;
-    if (!all_finite(a, n)) return RO_NONFINITE;
-    double *t = (double *)malloc(sizeof(double) * n);
-    if (!t) return RO_SHAPE;
-    for (int64_t d = 0; d < n; ++d) {
-        t[d] = qk * (double)a[d];  /* the logit of every pair at offset d */
-        if (!isfinite(t[d])) {
-            free(t);
-            return RO_NONFINITE;
-        }
-    }
-    for (int64_t i = 0; i < n; ++i) {
-        /* log Z_i from the sum shifted by the row maximum (every entry is live) */
-        double M = -INFINITY;
-        for (int64_t j = 0; j <= i; ++j)
-            if (t[i - j] > M) M = t[i - j];
-        double Zs = 0.0;
-        for (int64_t j = 0; j <= i; ++j) Zs += exp(t[i - j] - M);
-        const double logZ = M + log(Zs);
-        for (int64_t c = 0; c < dv; ++c) O[i * dv + c] = 0.0;
-        for (int64_t j = 0; j <= i; ++j) {
-            const double w = exp(t[i - j] - (beta == 0.0 ? 0.0 : beta * logZ));
-            for (int64_t c = 0; c < dv; ++c) O[i * dv + c] += w * (double)v[j * dv + c];
-        }
-    }
+    int rc;
+    double *t = position_logits(a, n, qk, &rc);
+    if (!t) return rc;
+    for (int64_t i = 0; i < n; ++i) position_row(t, v, i, dv, beta, O + i * dv);
+    free(t);
+    return RO_OK;
+}
+
+int ro_position_rows(const float *a, const float *v, int64_t n, int64_t dv, double beta,
+                     double qk, const int64_t *rows, int64_t nrows, double *O)
+{
+    if (n < 0 || dv <= 0 || nrows < 0) return RO_SHAPE;
+    for (int64_t k = 0; k < nrows; ++k)
+        if (rows[k] < 0 || rows[k] >= n) return RO_SHAPE;
+    if (nrows == 0) return RO_OK;
+    if (!isfinite(beta) || !isfinite(qk)) return RO_NONFINITE;
+    int rc;
+    double *t = position_logits(a, n, qk, &rc);
+    if (!t) return rc;
+    for (int64_t k = 0; k < nrows; ++k) position_row(t, v, rows[k], dv, beta, O + k * dv);
     free(t);
     return RO_OK;
 }

@@ -109,6 +109,11 @@ int ro_max_threads(void);
 int ro_position_head(const float *a, const float *v, int64_t n, int64_t dv, double beta,
                      double qk, double *O);
 
+/* Rows rows[0 .. nrows) of the same head (each 0 <= rows[k] < n), O [nrows, dv]: the same
+ * per-row arithmetic as ro_position_head, for sampled checks of long sequences. */
+int ro_position_rows(const float *a, const float *v, int64_t n, int64_t dv, double beta,
+                     double qk, const int64_t *rows, int64_t nrows, double *O);
+
 /* The same for BH heads: head h reads its offset logits at a + (h % H) * n (a [H,n], one
  * table per head index, shared across the batch), v [BH,n,dv], switches beta[h], qk[h];
  * O [BH,n,dv]. status[h] receives the head's code. Parallel over heads with OpenMP. */

@@ -511,6 +511,26 @@ def test_position_head_rows_sum_to_one_and_causal(R):
     assert not torch.equal(O1[:, :, 333:], O2[:, :, 333:])
 
 
+def test_position_workload_full_size_sampled_rows(R, oracle_mod):
+    """The benchmark's position workload (B=4 H=32 n=8192 dv=128, the launch it times):
+    sampled rows of 15 heads (first, tile edges, last) against the oracle row by row, with
+    the bound of the parity test above."""
+    pi = W.position()
+    B, H, n, dv = pi.B, pi.H, pi.n, pi.dv
+    O = R.position_head(dev(pi.a), dev(pi.v.reshape(B, H, n, dv), torch.bfloat16), pi.beta, pi.qk)
+    torch.cuda.synchronize()
+    Og = O.reshape(B * H, n, dv)
+    bq, qq = pi.switches_bh()[:2]
+    rows = [0, 1, 127, 128, 129, 255, 4095, 4096, 6143, 8063, 8190, 8191]
+    for bh in range(0, B * H, 9):
+        h = bh % H
+        got = Og[bh, rows].cpu().double().numpy()
+        ref = oracle_mod.position_rows(pi.a[h], pi.v[bh], float(bq[bh]), float(qq[bh]), rows)
+        absr = oracle_mod.position_rows(pi.a[h], np.abs(pi.v[bh]), float(bq[bh]), float(qq[bh]), rows)
+        bound = 2.0 ** -7 * absr + 1e-6 * (1.0 + np.max(absr))
+        assert np.all(np.abs(got - ref) <= bound), f"head {bh}: worst excess {np.max(np.abs(got - ref) - bound)}"
+
+
 def test_position_bounded_wait_reports_timeout(R, oracle_mod):
     """A block whose V loads stop after its first makes its tensor-core issuer's bounded wait
     run out (2 s): the status word says so, every block winds down (waiting for the copies

@@ -515,6 +515,24 @@ def test_position_head_closed_forms(oracle_mod):
     assert np.array_equal(O[:17], O2[:17]) and not np.array_equal(O[17:], O2[17:])
 
 
+def test_position_rows_are_rows_of_the_head(oracle_mod):
+    """The row-sampled evaluation (for long sequences) gives exactly the rows of the whole
+    head, at every switch setting, and refuses the same inputs."""
+    n = 57
+    a = rng(38).standard_normal(n).astype(np.float32)
+    v = rng(39).standard_normal((n, 3)).astype(np.float32)
+    rows = [0, 1, 17, 56, 33, 0]
+    for beta, qk in [(1.0, 1.0), (0.0, 0.5), (0.5, -0.75), (1.0, 0.0)]:
+        full = oracle_mod.position_head(a, v, beta, qk)
+        part = oracle_mod.position_rows(a, v, beta, qk, rows)
+        assert np.array_equal(part, full[rows])
+    bad = a.copy(); bad[40] = np.nan
+    with pytest.raises(oracle_mod.NonFinite):
+        oracle_mod.position_rows(bad, v, 1.0, 1.0, [3])
+    with pytest.raises(oracle_mod.ShapeError):
+        oracle_mod.position_rows(a, v, 1.0, 1.0, [n])
+
+
 def test_position_head_refusals_and_batching(oracle_mod):
     n = 12
     v = rng(36).standard_normal((n, 2)).astype(np.float32)
