@@ -89,6 +89,9 @@ def lib():
             L.ro_position_rows.argtypes = [_f32p, _f32p, _i64, _i64, _f64, _f64, _i64p, _i64,
                                            _f64p]
             L.ro_position_rows.restype = ctypes.c_int
+            L.ro_operator_rows.argtypes = [_f32p, _f32p, _f32p, _f32p, _i64, _i64, _f64, _f64,
+                                           _f64, _i64p, _i64, _f64p, _f64p]
+            L.ro_operator_rows.restype = ctypes.c_int
             L.ro_max_threads.argtypes = []
             L.ro_max_threads.restype = ctypes.c_int
             _lib = L
@@ -265,6 +268,21 @@ def chain_heads(u, theta, g, b, threads: int = 0):
     if rc == RO_SHAPE:
         raise ShapeError()
     return yr + 1j * yi, env, st
+
+
+def operator_rows(q, k, u, theta, beta: float, qk: float, g: float, rows) -> np.ndarray:
+    """Rows `rows` of W (same arithmetic as operator): [len(rows), n] complex."""
+    q = np.asarray(q, dtype=np.float32)
+    n = q.shape[0]
+    d = q.shape[1] if q.ndim == 2 else 0
+    qa, pq = _f32(q); ka, pk = _f32(k); ua, pu = _f32(u); ta, pt = _f32(theta)
+    if ka.size != n * d or ua.size != n or ta.size != n:
+        raise ShapeError()
+    rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    Wr = np.zeros((rr.size, n)); Wi = np.zeros((rr.size, n))
+    _raise(lib().ro_operator_rows(pq, pk, pu, pt, n, d, beta, qk, g, rr.ctypes.data_as(_i64p),
+                                  rr.size, _ptr64(Wr), _ptr64(Wi)))
+    return Wr + 1j * Wi
 
 
 def position_head(a, v, beta: float, qk: float) -> np.ndarray:

@@ -210,6 +210,34 @@ int ro_operator(const float *q, const float *k, const float *u, const float *the
     return rc;
 }
 
+int ro_operator_rows(const float *q, const float *k, const float *u, const float *theta,
+                     int64_t n, int64_t d, double beta, double qk, double g,
+                     const int64_t *rows, int64_t nrows, double *W_re, double *W_im)
+{
+    if (n < 0 || d <= 0 || nrows < 0) return RO_SHAPE;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= n) return RO_SHAPE;
+    if (nrows == 0) return RO_OK;
+    if (!switches_finite(beta, qk, g)) return RO_NONFINITE;
+    if (!all_finite(q, n * d) || !all_finite(k, n * d)) return RO_NONFINITE;
+
+    double *m = (double *)malloc(sizeof(double) * n);
+    double *a_re = (double *)malloc(sizeof(double) * n);
+    double *a_im = (double *)malloc(sizeof(double) * n);
+    row_scratch s;
+    int ok = m && a_re && a_im && scratch_alloc(&s, n);
+    int rc = ok ? head_gates(u, theta, g, n, m, NULL, a_re, a_im) : RO_SHAPE;
+    for (int64_t r = 0; rc == RO_OK && r < nrows; ++r) {
+        const int64_t i = rows[r];
+        double *wr = W_re + r * n, *wi = W_im + r * n;
+        for (int64_t j = i + 1; j < n; ++j) { wr[j] = 0.0; wi[j] = 0.0; } /* j > i */
+        rc = operator_row(q, k, m, a_re, a_im, d, i, beta, qk, &s, wr, wi);
+    }
+    if (ok) scratch_free(&s);
+    free(m); free(a_re); free(a_im);
+    return rc;
+}
+
 void ro_readout(const double *W_re, const double *W_im, const float *v,
                 int64_t n, int64_t dv, double *O_re, double *O_im)
 {

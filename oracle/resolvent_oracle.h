@@ -53,6 +53,12 @@ int ro_operator(const float *q, const float *k, const float *u, const float *the
                 int64_t n, int64_t d, double beta, double qk, double g,
                 double *W_re, double *W_im);
 
+/* Rows rows[0 .. nrows) of the same operator (each 0 <= rows[k] < n), W_re/W_im [nrows, n]:
+ * the same per-row arithmetic as ro_operator, for sampled checks at large n. */
+int ro_operator_rows(const float *q, const float *k, const float *u, const float *theta,
+                     int64_t n, int64_t d, double beta, double qk, double g,
+                     const int64_t *rows, int64_t nrows, double *W_re, double *W_im);
+
 /* Readout ("Object", readout row; Rust API `readout`): O_i = sum_j W_ij V_j. */
 void ro_readout(const double *W_re, const double *W_im, const float *v,
                 int64_t n, int64_t dv, double *O_re, double *O_im);

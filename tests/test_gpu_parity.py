@@ -446,6 +446,30 @@ def test_operator_matches_oracle(R, oracle_mod, case):
         assert np.all(np.triu(Wg[h], 1) == 0)
 
 
+def test_operator_workload_full_size_sampled_rows(R, oracle_mod):
+    """The benchmark's operator workload (B=1 H=8 n=4096 d=64, switches (1,1,0.5), the launch
+    it times): sampled rows of every head against the oracle's rows, with the bound and the
+    exact zero pattern of the test above."""
+    hi = W.WORKLOADS["operator"]()
+    B, H, n, d = hi.B, hi.H, hi.n, hi.d
+    shp = (B, H, n)
+    Wre, Wim = R.operator(dev(hi.q.reshape(*shp, d), torch.bfloat16),
+                          dev(hi.k.reshape(*shp, d), torch.bfloat16),
+                          dev(hi.u.reshape(shp)), dev(hi.theta.reshape(shp)), hi.beta, hi.qk, hi.g)
+    torch.cuda.synchronize()
+    rows = [0, 1, 127, 128, 129, 2047, 2048, 4094, 4095]
+    bq, qq, gg = [f32(x) for x in hi.switches_bh()]
+    for h in range(B * H):
+        got = (Wre.reshape(B * H, n, n)[h, rows].cpu().double().numpy()
+               + 1j * Wim.reshape(B * H, n, n)[h, rows].cpu().double().numpy())
+        ref = oracle_mod.operator_rows(hi.q[h], hi.k[h], hi.u[h], hi.theta[h], bq[h], qq[h], gg[h], rows)
+        scale = np.max(np.abs(ref))
+        assert np.max(np.abs(got - ref)) <= 1e-3 * scale, f"head {h}"
+        assert np.all(got[ref == 0] == 0), f"head {h}: zero pattern"
+        for r, i in enumerate(rows):
+            assert np.all(got[r, i + 1:] == 0)
+
+
 def test_operator_rows_are_stochastic(R):
     """beta = 1, real gates (theta = 0): every row of W sums to 1."""
     B, H, n, d = 1, 2, 520, 64

@@ -515,6 +515,26 @@ def test_position_head_closed_forms(oracle_mod):
     assert np.array_equal(O[:17], O2[:17]) and not np.array_equal(O[17:], O2[17:])
 
 
+def test_operator_rows_are_rows_of_the_operator(oracle_mod):
+    """The row-sampled operator (for large n) gives exactly the rows of the dense one, with
+    closed gates, complex phases and every switch corner, and refuses the same inputs."""
+    n, d = 45, 8
+    q = rng(40).standard_normal((n, d)).astype(np.float32)
+    k = rng(41).standard_normal((n, d)).astype(np.float32)
+    u = rng(42).uniform(-0.3, 1.2, n).astype(np.float32); u[[7, 30]] = 0.0
+    th = rng(43).uniform(-3.0, 3.0, n).astype(np.float32)
+    rows = [0, 1, 7, 8, 29, 31, 44, 8]
+    for beta, qk, g in [(1.0, 1.0, 0.5), (0.0, 1.0, 0.0), (0.0, 0.0, 1.0), (0.5, 0.7, 0.3)]:
+        full = oracle_mod.operator(q, k, u, th, beta, qk, g)
+        part = oracle_mod.operator_rows(q, k, u, th, beta, qk, g, rows)
+        assert np.array_equal(part, full[rows])
+    bad = q.copy(); bad[3, 2] = np.inf
+    with pytest.raises(oracle_mod.NonFinite):
+        oracle_mod.operator_rows(bad, k, u, th, 1.0, 1.0, 0.5, [5])
+    with pytest.raises(oracle_mod.ShapeError):
+        oracle_mod.operator_rows(q, k, u, th, 1.0, 1.0, 0.5, [-1])
+
+
 def test_position_rows_are_rows_of_the_head(oracle_mod):
     """The row-sampled evaluation (for long sequences) gives exactly the rows of the whole
     head, at every switch setting, and refuses the same inputs."""
