@@ -10,13 +10,16 @@
 //            (the tensor-core operand); C(i) = sum_{d<=i} kappa(d) over the rounded values, so
 //            that the weights of a row sum to exactly what divides them; and the last offset
 //            whose kappa is not 0;
-//   main  -- one CTA per 128-row query tile: O_tile = sum_delta P(delta) V(QB - delta), P(delta)
-//            the 128 x 128 block-Toeplitz tile P[r][c] = kappa(128 delta + r - c) (0 for a
-//            negative offset or one past n). Builder warps write P into TMEM from a segment of
-//            kappa staged in shared memory (no logits, no exponential per entry); one thread
-//            issues P V (tcgen05.mma, P from TMEM, V by TMA); tiles whose offsets all lie past
-//            the last nonzero kappa are skipped. The epilogue divides by C(i)^beta, multiplies
-//            by e^{(1-beta) M}, and writes O with coalesced 16-byte stores.
+//   main  -- one CTA per pair of 128-row query tiles: O_tile = sum_delta P(delta) V(Q - delta),
+//            P(delta) the 128 x 128 block-Toeplitz tile P[r][c] = kappa(128 delta + r - c) (0
+//            for a negative offset or one past n). Builder warps write P into shared memory
+//            from the bf16 kappa table (no logits, no exponential per entry); one thread issues
+//            the products transposed, O^T += V^T P^T (tcgen05.mma, V by TMA), so that both tiles
+//            of the pair share each V tile; blocks whose offsets all lie past the last nonzero
+//            kappa are skipped. The epilogue divides by C(i)^beta, multiplies by e^{(1-beta) M},
+//            and writes O with coalesced 16-byte stores.
+//            P stays out of TMEM: stores into TMEM from threads are starved while the tensor
+//            pipe runs, so a P block written there would wait for the pipe's gaps.
 #include "head_common.cuh"
 
 namespace rs {
