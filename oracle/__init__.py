@@ -9,8 +9,8 @@ Every routine follows "Resolvent Operator" (teerth.dev/Aether-Lang/integrated/re
 section "Object" and section "Evaluation and refusals". Inputs are passed as fp32 arrays
 holding the same stored values the GPU reads (bf16 and fp32 both widen to fp64 exactly).
 
-Parity status: beta strictly inside (0,1) is "parity unpinned" (the pages make no statement
-there); every other regime is pinned by the CPU tests.
+Parity status: every regime is pinned by the CPU tests; for beta strictly inside (0,1), where
+the pages give no value, by the closed forms of constant logits and W(beta) Z^beta = W(0).
 """
 from __future__ import annotations
 

@@ -21,8 +21,9 @@
  *  - a logit is refused when non-finite on any causal entry j <= i, live or not; with
  *    qk = 0 the dot product is not evaluated, so it cannot overflow (the pages accept it).
  *  - the chain starts at y_0 = b_0 (the page's y_0 = 0 is the case b_0 = 0).
- * Parity status: beta strictly inside (0,1) is "parity unpinned" -- the pages say nothing
- * there; the tests check only W(beta) * Z^beta = W(0).
+ * Parity status: beta strictly inside (0,1) -- the pages give no value there; the tests pin
+ * the closed forms of constant logits (W_ij = (i+1)^-beta for q = 0 and open gates, and the
+ * constant-logit position head) and W(beta) * Z^beta = W(0).
  *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (contraction off so that x86 and
  * Arm builds round identically).

@@ -20,9 +20,9 @@
  * which the pages' Rust module signals by panicking).
  *
  * Parity status: every routine is pinned by the CPU test suite against closed forms,
- * library routines and the pages' printed values, except the operator for beta strictly
- * inside (0,1): the pages make no statement there, so that regime is "parity unpinned"
- * (it is checked only for self-consistency: W(beta) * Z^beta == W(0)).
+ * library routines and the pages' printed values. For beta strictly inside (0,1), where the
+ * pages give no value, the pins are the closed forms of constant logits (W_ij = (i+1)^-beta
+ * for q = 0 and open gates; the constant-logit position head) and W(beta) * Z^beta == W(0).
  */
 #ifndef RESOLVENT_ORACLE_H
 #define RESOLVENT_ORACLE_H

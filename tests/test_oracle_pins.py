@@ -515,6 +515,30 @@ def test_position_head_closed_forms(oracle_mod):
     assert np.array_equal(O[:17], O2[:17]) and not np.array_equal(O[17:], O2[17:])
 
 
+@pytest.mark.parametrize("beta", [0.25, 0.5, 0.75])
+def test_intermediate_beta_closed_forms(oracle_mod, beta):
+    """beta strictly inside (0, 1), where W = G e^{qk s} / Z^beta has closed forms when every
+    logit is the same: with q = 0 and open gates (g = 0), Z_i = i + 1 and
+    W_ij = (i + 1)^-beta; a position-only head with constant logits c gives
+    O_i = e^{qk c (1 - beta)} (i + 1)^-beta sum_{j<=i} v_j. A wrong exponent (Z^{1-beta},
+    Z^-beta left out, or beta applied to the shift) fails them."""
+    n, d = 24, 8
+    q = np.zeros((n, d), np.float32)
+    k = rng(44).standard_normal((n, d)).astype(np.float32)
+    u = rng(45).uniform(0.0, 1.0, n).astype(np.float32)
+    th = rng(46).uniform(-3.0, 3.0, n).astype(np.float32)
+    Wm = oracle_mod.operator(q, k, u, th, beta, 0.7, 0.0)
+    i = np.arange(n)[:, None].astype(np.float64)
+    expect = np.tril(np.ones((n, n))) * (i + 1.0) ** -beta
+    assert np.max(np.abs(Wm - expect)) <= 1e-14
+    v = rng(47).standard_normal((n, 3)).astype(np.float32).astype(np.float64)
+    c = np.full(n, -1.25, np.float32)
+    qk = 0.8
+    O = oracle_mod.position_head(c, v, beta, qk)
+    ref = math.exp(qk * -1.25 * (1.0 - beta)) * (i + 1.0) ** -beta * np.cumsum(v, 0)
+    assert np.max(np.abs(O - ref)) <= 1e-12 * (1.0 + np.max(np.abs(ref)))
+
+
 def test_operator_rows_are_rows_of_the_operator(oracle_mod):
     """The row-sampled operator (for large n) gives exactly the rows of the dense one, with
     closed gates, complex phases and every switch corner, and refuses the same inputs."""
