@@ -60,3 +60,40 @@ def test_host_argument_checks_without_a_gpu(built_lib):
     assert L.resolvent_head_workspace_bytes(1, 2, 0, 64, 64, R.RS_BF16) == 0
     assert L.resolvent_head_workspace_bytes(2, 3, 300, 64, 64, R.RS_BF16) > 2 * 3 * 300 * 24
     assert L.resolvent_status_string(R.RS_ERR_NONFINITE) == b"non-finite input refused"
+
+
+def test_operator_and_position_argument_checks_without_a_gpu(built_lib):
+    """The operator and position-head entry points answer shape, support, switch, alignment
+    and workspace errors on the host, before any CUDA call (pointer values are only
+    inspected, never dereferenced)."""
+    import gated_causal_attention_gb300 as R
+    L = R.lib()
+    A, M = 0x10000, 0x10004  # a 16-byte-aligned and a misaligned address (never dereferenced)
+    sw, keep = R._switches(2, 1.0, 1.0, 0.5)
+    sw0, keep0 = R._switches(2, 1.0, 1.0, 0.0)
+    # operator: empty call; d = 0; d not a multiple of 8; misaligned; workspace too small
+    op = lambda n, d, q, ws, wsb, s=sw: L.resolvent_operator(q, A, A, A, s, 1, 2, n, d, R.RS_BF16,
+                                                              A, A, ws, wsb, A, None)
+    assert op(0, 64, A, A, 0) == R.RS_OK
+    assert op(5, 0, A, A, 0) == R.RS_ERR_SHAPE
+    assert op(5, 60, A, A, 0) == R.RS_ERR_UNSUPPORTED
+    assert op(5, 64, M, A, 1 << 30) == R.RS_ERR_ALIGN
+    need = L.resolvent_operator_workspace_bytes(1, 2, 300, 64, R.RS_BF16)
+    assert need > 0 and L.resolvent_operator_workspace_bytes(1, 2, 0, 64, R.RS_BF16) == 0
+    assert op(300, 64, A, A, need - 1) == R.RS_ERR_WORKSPACE
+    assert op(300, 64, A, None, 0) == R.RS_ERR_WORKSPACE
+    # position heads: empty call; dv = 0 or above 128; a gate switch other than 0;
+    # misaligned; workspace too small
+    pos = lambda n, dv, v, ws, wsb, s=sw0: L.resolvent_position_head(A, v, s, 1, 2, n, dv, R.RS_BF16,
+                                                                     A, ws, wsb, A, None)
+    assert pos(0, 64, A, A, 0) == R.RS_OK
+    assert pos(5, 0, A, A, 0) == R.RS_ERR_SHAPE
+    assert pos(5, 256, A, A, 0) == R.RS_ERR_UNSUPPORTED
+    assert pos(5, 64, A, A, 1 << 30, s=sw) == R.RS_ERR_UNSUPPORTED
+    assert pos(5, 64, M, A, 1 << 30) == R.RS_ERR_ALIGN
+    needp = L.resolvent_position_workspace_bytes(1, 2, 300, 64, R.RS_BF16)
+    assert needp > 0 and L.resolvent_position_workspace_bytes(1, 2, 0, 64, R.RS_BF16) == 0
+    assert pos(300, 64, A, A, needp - 1) == R.RS_ERR_WORKSPACE
+    bad, keepb = R._switches(2, float("inf"), 1.0, 0.0)
+    assert pos(5, 64, A, A, 1 << 30, s=bad) == R.RS_ERR_NONFINITE
+
