@@ -88,3 +88,30 @@ def test_work_accounting_stops_at_fp32_underflow():
     # than the exact product: the count is exact-arithmetic, so never above the fp32 one
     got = bench.live_entries(u, 1.0)
     assert got <= cnt and cnt - got <= 0.01 * cnt
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle timed on the host cores) prints exactly one JSON
+    line with the keys the driver reads, for the head and the position-only workloads."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for wl in ("tiny", "position"):
+        args = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                "--workload", wl, "--steps", "1", "--warmup", "0", "--cpu-seconds", "0.2"]
+        if wl == "position":
+            args += ["--B", "1", "--H", "2", "--n", "512"]
+        out = subprocess.run(args, capture_output=True, text=True, timeout=300, cwd=root)
+        assert out.returncode == 0, out.stderr[-2000:]
+        lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]
+        assert len(lines) == 1
+        d = json.loads(lines[0])
+        for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                  "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                  "cpu_baseline", "e2e"):
+            assert k in d, k
+        assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
+        assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+        assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+        assert d["config"]["workload"] == wl
