@@ -660,3 +660,35 @@ def test_chain_heads_matches_single_chain(oracle_mod):
         yh, eh = oracle_mod.chain(gates_of(oracle_mod, u[h], th[h], g), b[h], with_envelope=True)
         assert np.array_equal(y[h], yh) and np.array_equal(env[h], eh)
         assert np.all(np.abs(yh) <= eh * (1 + 1e-12) + 1e-300)
+
+
+def test_chain_envelope_is_the_chain_of_moduli(oracle_mod):
+    """The forward-error envelope that scales every GPU chain tolerance,
+    env_i = |a_i| env_{i-1} + |b_i|, is the same chain over the reals with |a| and |b|
+    ("Resolvent Operator", Lean table, `CEQ.V15Fork.chain_eq_sum`: the chain is
+    sum_{s<=i} (prod_{k=s+1..i} a_k) b_s): env_i = sum_{s<=i} R_is |b_s| with R_is the modulus of
+    the path product (pinned to the Neumann resolvent above), to 1e-12. For one constant gate
+    it is the first-order IIR filter of |b| with pole |a| (scipy's lfilter)."""
+    n, dv = 60, 3
+    r = rng(27)
+    for g, lo in ((1.0, 0.7), (0.5, -0.3), (0.0, 0.0)):
+        u = r.uniform(lo, 1.0, n).astype(np.float32)
+        u[r.choice(n, 3, replace=False)] = 0.0
+        th = r.uniform(-3, 3, n).astype(np.float32)
+        b = r.standard_normal((n, dv)).astype(np.float32)
+        a = gates_of(oracle_mod, u, th, g)
+        _, env = oracle_mod.chain(a, b, with_envelope=True)
+        R = np.abs(oracle_mod.path_product(a))
+        want = np.tril(R) @ np.abs(b.astype(np.float64))
+        assert np.max(np.abs(env - want) / np.maximum(want, 1e-300)) <= 1e-12, g
+        # the batched routine returns the same envelope
+        _, env_b, st = oracle_mod.chain_heads(u[None], th[None], [g], b[None])
+        assert st[0] == 0 and np.array_equal(env_b[0], env)
+    # one constant gate of modulus 0.9 and any phase
+    a0 = 0.9 * np.exp(1j * 0.7)
+    b = r.standard_normal((200, dv)).astype(np.float32)
+    a = np.full(200, a0)
+    _, env = oracle_mod.chain(a, b, with_envelope=True)
+    for c in range(dv):
+        ref = scipy.signal.lfilter([1.0], [1.0, -abs(a0)], np.abs(b[:, c].astype(np.float64)))
+        assert np.max(np.abs(env[:, c] - ref) / ref) <= 1e-12
