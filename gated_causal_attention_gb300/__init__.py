@@ -106,10 +106,17 @@ def lib() -> ctypes.CDLL:
         L.resolvent_test_set_chain_withhold.restype = None
         L.resolvent_test_set_position_withhold.argtypes = [_I]
         L.resolvent_test_set_position_withhold.restype = None
+        L.resolvent_test_set_head_withhold.argtypes = [_I]
+        L.resolvent_test_set_head_withhold.restype = None
+        L.resolvent_test_set_operator_withhold.argtypes = [_I, _I]
+        L.resolvent_test_set_operator_withhold.restype = None
         L.resolvent_profile_enable.argtypes = [_I]
         L.resolvent_profile_enable.restype = _I
         L.resolvent_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_float), _I]
         L.resolvent_profile_collect.restype = _I
+        L.resolvent_profile_collect_kinds.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                                      ctypes.POINTER(ctypes.c_int), _I]
+        L.resolvent_profile_collect_kinds.restype = _I
         _lib = L
     return _lib
 
@@ -373,15 +380,32 @@ def test_set_position_withhold(block: int) -> None:
     lib().resolvent_test_set_position_withhold(int(block))
 
 
+def test_set_head_withhold(block: int) -> None:
+    lib().resolvent_test_set_head_withhold(int(block))
+
+
+def test_set_operator_withhold(launch: int, block: int) -> None:
+    """launch 0: the row statistics, 1: the write of W; block -1 turns the knob off."""
+    lib().resolvent_test_set_operator_withhold(int(launch), int(block))
+
+
 def profile_enable(on: bool = True) -> None:
     """Record CUDA events around the main kernel of every following call."""
     _raise(lib().resolvent_profile_enable(1 if on else 0))
 
 
-def profile_collect(max_pairs: int = 1024) -> list:
-    """Durations (ms) of the kernels recorded since profiling was enabled or last collected."""
+PROF_HEAD_GATED, PROF_HEAD_REAL, PROF_READOUT, PROF_CHAIN = 0, 1, 2, 3
+PROF_OPERATOR, PROF_POSITION, PROF_GATE_PREP = 4, 5, 6
+
+
+def profile_collect(max_pairs: int = 4096, kinds: bool = False) -> list:
+    """Durations (ms) of the launches recorded since profiling was enabled or last collected;
+    with kinds=True, (ms, class) pairs (PROF_* above)."""
     buf = (ctypes.c_float * max_pairs)()
-    k = lib().resolvent_profile_collect(buf, max_pairs)
+    kb = (ctypes.c_int * max_pairs)()
+    k = lib().resolvent_profile_collect_kinds(buf, kb, max_pairs)
     if k < 0:
         raise ResolventError(RS_ERR_CUDA, "profile collection failed")
+    if kinds:
+        return [(float(buf[i]), int(kb[i])) for i in range(k)]
     return [float(buf[i]) for i in range(k)]

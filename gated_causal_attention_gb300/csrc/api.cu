@@ -20,22 +20,26 @@ thread_local int g_launches = 0;
 uint64_t g_wait_limit_ns = kWaitLimitNs;
 int g_chain_withhold = -1;
 int g_position_withhold = -1;
+int g_head_withhold = -1;
+int g_operator_withhold_stats = -1, g_operator_withhold_write = -1;
 
-// Optional timing of the main kernel of each call (the fused head, or the chain scan when
-// a call has no other heads): a ring of CUDA event pairs recorded on the caller's stream.
-constexpr int kProfSlots = 1024;
+// Optional timing of the main kernels of each call: CUDA event pairs recorded on the caller's
+// stream around each class of launch (RS_PROF_* in resolvent.h), kept in order.
+constexpr int kProfSlots = 4096;
 struct Prof {
     bool on = false;
     int next = 0;
     cudaEvent_t ev[kProfSlots][2];
+    int kind[kProfSlots];
     bool made = false;
 } g_prof;
 std::mutex g_prof_mu;
 
-void prof_mark(cudaStream_t s, int which)
+void prof_mark(cudaStream_t s, int which, int kind)
 {
     if (!g_prof.on || g_prof.next >= kProfSlots) return;
     cudaEventRecord(g_prof.ev[g_prof.next][which], s);
+    g_prof.kind[g_prof.next] = kind;
     if (which == 1) ++g_prof.next;
 }
 
@@ -200,7 +204,7 @@ ChainWs chain_ws(void *base, int slots, int n, int dv)
 
 rs_status run_chain(const std::vector<HeadTable> &tabs, const float *u, const float *theta,
                     const void *b, int b_is_bf16, int n, int dv, float *y_re, float *y_im,
-                    void *scratch, int32_t *status, cudaStream_t s, bool profile, bool normalize = false,
+                    void *scratch, int32_t *status, cudaStream_t s, int prof_kind, bool normalize = false,
                     const float2 *carry_in = nullptr, float2 *carry_out = nullptr)
 {
     for (size_t i = 0; i < tabs.size(); ++i) {
@@ -215,9 +219,9 @@ rs_status run_chain(const std::vector<HeadTable> &tabs, const float *u, const fl
         a.normalize = normalize ? 1 : 0; a.agg_z = w.agg_z; a.incl_z = w.incl_z;
         a.carry_in = carry_in; a.carry_out = carry_out;
         a.wait_limit_ns = g_wait_limit_ns; a.withhold_chunk = g_chain_withhold;
-        if (profile && i == 0) prof_mark(s, 0);
+        if (i == 0) prof_mark(s, 0, prof_kind);
         e = launch_chain_scan(a, t, s);
-        if (profile && i + 1 == tabs.size()) prof_mark(s, 1);
+        if (i + 1 == tabs.size()) prof_mark(s, 1, prof_kind);
         ++g_launches;
         if (e != cudaSuccess) return RS_ERR_CUDA;
     }
@@ -261,6 +265,7 @@ rs_status resolvent_gate_prep(const float *u, const float *theta, rs_switches sw
                           (const void *)block_carry})
         if (p && !aligned16(p)) return RS_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_mark(s, 0, RS_PROF_GATE_PREP);
     for (const HeadTable &t : tables_for(sw, B, H, [](const Sw &) { return true; })) {
         GatePrepArgs a{};
         a.u = u; a.theta = theta; a.n = n; a.m = m; a.theta_p = theta_p;
@@ -272,6 +277,7 @@ rs_status resolvent_gate_prep(const float *u, const float *theta, rs_switches sw
         if (launch_gate_prep(a, t, s) != cudaSuccess) return RS_ERR_CUDA;
         ++g_launches;
     }
+    prof_mark(s, 1, RS_PROF_GATE_PREP);
     return RS_OK;
 }
 
@@ -365,6 +371,7 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
             ha.carry = carry; ha.O_re = O_re; ha.O_im = O_im; ha.status = status_dev;
             ha.tma_out = tma_out ? 1 : 0;
             ha.numkv = reinterpret_cast<int *>(ws + w.numkv);
+            ha.withhold = g_head_withhold;
             // about 24 MB of K and V per head group: a group's K/V tiles stay in L2
             const size_t kv_head = (size_t)n * (DP + DVP) * 2;
             ha.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / kv_head));
@@ -379,22 +386,23 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
         }
         // The per-tile key-tile counts share one scratch array, so each table's count runs
         // right before its head launch (same stream).
-        prof_mark(s, 0);
         for (size_t i = 0; i < head_tabs.size(); ++i) {
+            const int kind = head_tabs[i].g[0] != 0.f ? RS_PROF_HEAD_GATED : RS_PROF_HEAD_REAL;
+            prof_mark(s, 0, kind);
             if (head_tabs[i].g[0] != 0.f) {
                 if (launch_head_numkv(args[i], head_tabs[i], s) != cudaSuccess) return RS_ERR_CUDA;
                 ++g_launches;
             }
             if (launch_head_fwd(args[i], head_tabs[i], maps, DP, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
+            prof_mark(s, 1, kind);
             ++g_launches;
         }
-        prof_mark(s, 1);
     }
 
     // qk = 0 and beta = 0: W = G exactly, so O is the chain over V.
     if (!chain_tabs.empty()) {
         st = run_chain(chain_tabs, u, theta, v, f32 ? 0 : 1, n, dv, O_re, O_im, ws + w.chain,
-                       status_dev, s, head_tabs.empty(), true);
+                       status_dev, s, RS_PROF_READOUT, true);
         if (st != RS_OK) return st;
     }
     return RS_OK;
@@ -502,10 +510,12 @@ rs_status resolvent_operator(const void *q, const void *k, const float *u, const
         oa.rowf = reinterpret_cast<float4 *>(ws + w.rowf);
         oa.rowq = reinterpret_cast<float *>(ws + w.rowq);
         oa.status = status_dev; oa.tma_out = tma_out ? 1 : 0;
+        oa.withhold_stats = g_operator_withhold_stats;
+        oa.withhold_write = g_operator_withhold_write;
         if (launch_operator_stats(oa, t, maps, DP, s) != cudaSuccess) return RS_ERR_CUDA;
-        prof_mark(s, 0);
+        prof_mark(s, 0, RS_PROF_OPERATOR);
         if (launch_operator(oa, t, maps, DP, s) != cudaSuccess) return RS_ERR_CUDA;
-        prof_mark(s, 1);
+        prof_mark(s, 1, RS_PROF_OPERATOR);
         g_launches += 3;
     }
     return RS_OK;
@@ -588,9 +598,9 @@ rs_status resolvent_position_head(const float *a, const void *v, rs_switches sw,
         // about 24 MB of V per head group: a group's V tiles stay in L2
         const size_t v_head = (size_t)n * DVP * 2;
         pa.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / v_head));
-        prof_mark(s, 0);
+        prof_mark(s, 0, RS_PROF_POSITION);
         if (launch_position_head(pa, t, maps, DVP, s) != cudaSuccess) return RS_ERR_CUDA;
-        prof_mark(s, 1);
+        prof_mark(s, 1, RS_PROF_POSITION);
         g_launches += 2;
     }
     return RS_OK;
@@ -621,7 +631,7 @@ rs_status resolvent_chain_scan(const float *u, const float *theta, rs_switches s
     if (!workspace || workspace_bytes < resolvent_chain_workspace_bytes(B, H, n, dv))
         return RS_ERR_WORKSPACE;
     return run_chain(tables_for(sw, B, H, [](const Sw &) { return true; }), u, theta, b, 0, n, dv,
-                     y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), true);
+                     y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), RS_PROF_CHAIN);
 }
 
 rs_status resolvent_chain_scan_carry(const float *u, const float *theta, rs_switches sw,
@@ -646,7 +656,7 @@ rs_status resolvent_chain_scan_carry(const float *u, const float *theta, rs_swit
         return RS_ERR_WORKSPACE;
     // the tables hold at most kMaxSlots heads each; carries are indexed by (b, h) directly
     return run_chain(tables_for(sw, B, H, [](const Sw &) { return true; }), u, theta, b, 0, n, dv,
-                     y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), true,
+                     y_re, y_im, workspace, status_dev, static_cast<cudaStream_t>(stream), RS_PROF_CHAIN,
                      false, reinterpret_cast<const float2 *>(carry_in),
                      reinterpret_cast<float2 *>(carry_out));
 }
@@ -671,7 +681,7 @@ rs_status resolvent_chain_scan_noalloc(const float *u, const float *theta, rs_sw
     void *scratch = nullptr;
     if (chain_noalloc_scratch(&scratch) != cudaSuccess) return RS_ERR_CUDA;
     return run_chain(tables_for(sw, B, H, [](const Sw &) { return true; }), u, theta, b, 0, n, dv,
-                     y_re, y_im, scratch, status_dev, static_cast<cudaStream_t>(stream), true);
+                     y_re, y_im, scratch, status_dev, static_cast<cudaStream_t>(stream), RS_PROF_CHAIN);
 }
 
 rs_status resolvent_status_sync(int32_t *status_dev, void *stream)
@@ -682,8 +692,9 @@ rs_status resolvent_status_sync(int32_t *status_dev, void *stream)
         return RS_ERR_CUDA;
     if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), s) != cudaSuccess) return RS_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
-    if (host & RS_STATUS_NONFINITE) return RS_ERR_NONFINITE;
+    // after a timeout the outputs, and a refusal raised from them, mean nothing: it comes first
     if (host & RS_STATUS_TIMEOUT) return RS_ERR_TIMEOUT;
+    if (host & RS_STATUS_NONFINITE) return RS_ERR_NONFINITE;
     return RS_OK;
 }
 
@@ -726,6 +737,12 @@ rs_status resolvent_debug_path_product(const float *u, const float *theta, rs_sw
 void resolvent_test_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns ? ns : kWaitLimitNs; }
 void resolvent_test_set_chain_withhold(int ticket) { g_chain_withhold = ticket; }
 void resolvent_test_set_position_withhold(int block) { g_position_withhold = block; }
+void resolvent_test_set_head_withhold(int block) { g_head_withhold = block; }
+void resolvent_test_set_operator_withhold(int launch, int block)
+{
+    g_operator_withhold_stats = launch == 0 ? block : -1;
+    g_operator_withhold_write = launch == 1 ? block : -1;
+}
 
 rs_status resolvent_profile_enable(int on)
 {
@@ -741,16 +758,19 @@ rs_status resolvent_profile_enable(int on)
     return RS_OK;
 }
 
-int resolvent_profile_collect(float *ms, int max)
+int resolvent_profile_collect_kinds(float *ms, int *kind, int max)
 {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     int k = 0;
     for (; k < g_prof.next && k < max; ++k) {
         if (cudaEventSynchronize(g_prof.ev[k][1]) != cudaSuccess) return -1;
         if (cudaEventElapsedTime(&ms[k], g_prof.ev[k][0], g_prof.ev[k][1]) != cudaSuccess) return -1;
+        if (kind) kind[k] = g_prof.kind[k];
     }
     g_prof.next = 0;
     return k;
 }
+
+int resolvent_profile_collect(float *ms, int max) { return resolvent_profile_collect_kinds(ms, nullptr, max); }
 
 }  // extern "C"

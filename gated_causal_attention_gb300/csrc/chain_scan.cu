@@ -400,26 +400,63 @@ cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 }  // namespace
 
 // Scratch of resolvent_chain_scan_noalloc: one fixed array in device memory, reserved when
-// the library is loaded on a device and held until the process exits. Host code must not
-// pass `g_chain_noalloc_scratch` itself to a kernel (on the host it names a stand-in, not a
-// device address); chain_noalloc_scratch() looks up the device address once per device.
+// the library's device code is loaded in a context (with lazy module loading, at the first
+// call that needs it) and held until the process exits. Host code must not pass
+// `g_chain_noalloc_scratch` itself to a kernel (on the host it names a stand-in, not a
+// device address); chain_noalloc_scratch() looks up the device address once per device and
+// context: a context made after cudaDeviceReset holds a new copy of the array, so the
+// address is looked up again when the current context's id changes.
 static __device__ __align__(256) unsigned char g_chain_noalloc_scratch[kChainNoAllocBytes];
+
+namespace {
+// cuCtxGetId through the runtime's driver entry point (no link against libcuda)
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+bool current_context_id(unsigned long long *id)
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+}  // namespace
 
 cudaError_t chain_noalloc_scratch(void **ptr)
 {
     constexpr int kMaxDevices = 64;
     static void *addr[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
     static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // cudaSetDevice makes the device's primary context current (creating it on first use),
+    // so that its id can be read before the first launch
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) return cudaErrorDeviceUninitialized;
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || ctx_of[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_chain_noalloc_scratch);  // with `dev` current
         if (e != cudaSuccess) return e;
         addr[dev] = p;
+        ctx_of[dev] = ctx;
     }
     *ptr = addr[dev];
     return cudaSuccess;

@@ -90,6 +90,33 @@ gate_prep_kernel(GatePrepArgs a, const __grid_constant__ HeadTable tab)
     if (lane == 31) later = {1.f, 0.f};
     const cplx block_total = shfl_idx(incl, 31);
 
+    if ((n & 3) == 0 && t0 + kTokPerLane <= n) {
+        // whole 16-byte units: a lane's four tokens are contiguous and 16-byte aligned
+        if (a.m) *reinterpret_cast<float4 *>(a.m + base + t0) = make_float4(mm[0], mm[1], mm[2], mm[3]);
+        if (a.theta_p)
+            *reinterpret_cast<float4 *>(a.theta_p + base + t0) = make_float4(tp[0], tp[1], tp[2], tp[3]);
+        if (a.gate) {
+            float4 *gp = reinterpret_cast<float4 *>(a.gate + base + t0);
+            gp[0] = make_float4(gt[0].re, gt[0].im, gt[1].re, gt[1].im);
+            gp[1] = make_float4(gt[2].re, gt[2].im, gt[3].re, gt[3].im);
+        }
+        if (a.prefix) {
+            cplx p[kTokPerLane];
+#pragma unroll
+            for (int k = 0; k < kTokPerLane; ++k) p[k] = cmul(excl, lp[k]);
+            float4 *pp = reinterpret_cast<float4 *>(a.prefix + base + t0);
+            pp[0] = make_float4(p[0].re, p[0].im, p[1].re, p[1].im);
+            pp[1] = make_float4(p[2].re, p[2].im, p[3].re, p[3].im);
+        }
+        if (a.suffix) {
+            cplx q[kTokPerLane];
+#pragma unroll
+            for (int k = 0; k < kTokPerLane; ++k) q[k] = cmul(ls[k], later);
+            float4 *sp = reinterpret_cast<float4 *>(a.suffix + base + t0);
+            sp[0] = make_float4(q[0].re, q[0].im, q[1].re, q[1].im);
+            sp[1] = make_float4(q[2].re, q[2].im, q[3].re, q[3].im);
+        }
+    } else {
 #pragma unroll
     for (int k = 0; k < kTokPerLane; ++k) {
         const int t = t0 + k;
@@ -105,6 +132,7 @@ gate_prep_kernel(GatePrepArgs a, const __grid_constant__ HeadTable tab)
             const cplx s = cmul(ls[k], later);
             a.suffix[base + t] = make_float2(s.re, s.im);
         }
+    }
     }
     if (a.carry && lane == 0)
         a.carry[bh * nb + blk] = make_float2(block_total.re, block_total.im);

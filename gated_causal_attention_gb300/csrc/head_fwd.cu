@@ -222,6 +222,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int st = t % L::NSK;
+                if (t == 1 && (int)blockIdx.x == a.withhold) break;  // test knob (timeout path)
                 if (t >= L::NSK && !wait_bar(B.empty + st, ((t / L::NSK) - 1) & 1, s_abort, a.status, 256)) break;
                 const int kb = t < numkv ? QB - 1 - t : QB;
                 unsigned char *stg = smem + L::stages + st * L::k_bytes;
@@ -235,6 +236,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int st = t % NS;
+                if (t == 1 && (int)blockIdx.x == a.withhold) break;  // test knob (timeout path)
                 if (t >= NS && !wait_bar(B.empty + st, ((t / NS) - 1) & 1, s_abort, a.status, 256)) break;
                 const int kb = t < numkv ? QB - 1 - t : QB;
                 unsigned char *stg = smem + L::stages + st * L::stage_bytes;
@@ -254,6 +256,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int sv = t % L::NSV;
+                if (t == 1 && (int)blockIdx.x == a.withhold) break;  // test knob (timeout path)
                 if (t >= L::NSV && !wait_bar(B.vempty + sv, ((t / L::NSV) - 1) & 1, s_abort, a.status, 256)) break;
                 const int kb = t < numkv ? QB - 1 - t : QB;
                 unsigned char *stg = smem + L::vring + sv * L::v_bytes;
@@ -749,7 +752,9 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
         }
 
         // the second half hands its partial sum to the first, which works out the output
-        // factor f = e^{(1-beta) M} Z'^{-beta} and the refusal; both halves then write O
+        // factor e^{(1-beta) M} Z'^{-beta} and the refusal; both halves then write O. The factor
+        // is applied as two equal halves f = 2^{E/2}, O = (acc f) f, so that an output whose
+        // value is within fp32 is not lost to a factor that alone overflows (or underflows).
         if (h == 1) s_zpart[r] = Zs + chk;  // chk is 0, or NaN to refuse
         ok = named_bar_and(kBarRows0 + (warp & 3), 64, ok && !*s_abort);
         if (h == 0) {
@@ -758,7 +763,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
             float f = 0.f;
             if (valid) {
                 bad = isnan(chk) || !isfinite(M2) || !(Zs > 0.f) || !isfinite(Zs);
-                f = (beta == 0.f) ? exp2f(M2) : exp2f((1.f - beta) * M2 - beta * log2f(Zs));
+                const float E = (beta == 0.f) ? M2 : (1.f - beta) * M2 - beta * log2f(Zs);
+                f = exp2f(0.5f * E);
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
             s_zpart[r] = f;
@@ -791,10 +797,10 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const float xr = __uint_as_float(re[4 * c + k]);
-                                wr[k] = __float_as_uint(xr == 0.f ? 0.f : xr * f);  // an exact 0 stays 0
+                                wr[k] = __float_as_uint(xr == 0.f ? 0.f : (xr * f) * f);  // an exact 0 stays 0
                                 if (GATED) {
                                     const float xi = __uint_as_float(im[4 * c + k]);
-                                    wi[k] = __float_as_uint(xi == 0.f ? 0.f : xi * f);
+                                    wi[k] = __float_as_uint(xi == 0.f ? 0.f : (xi * f) * f);
                                 }
                             }
                             sts128(stage_re + off, make_uint4(wr[0], wr[1], wr[2], wr[3]));
@@ -846,8 +852,8 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                         if (valid && 32 * q + e < a.dv) {
                             const float xr = __uint_as_float(re[e]);
                             const float xi = GATED ? __uint_as_float(im[e]) : 0.f;
-                            ore[32 * q + e] = (xr == 0.f) ? 0.f : xr * f;
-                            oim[32 * q + e] = (xi == 0.f) ? 0.f : xi * f;
+                            ore[32 * q + e] = (xr == 0.f) ? 0.f : (xr * f) * f;
+                            oim[32 * q + e] = (xi == 0.f) ? 0.f : (xi * f) * f;
                         }
                 }
             }

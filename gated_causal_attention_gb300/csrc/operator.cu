@@ -199,7 +199,8 @@ __device__ __forceinline__ void fetch_cols(const OpArgs &a, int64_t tok0, int QB
 template <int DP, bool GATED, class L, class RowData>
 __device__ __forceinline__ bool produce_tile(const OpArgs &a, const OpMaps &maps, const OpSmem &m,
                                              uint32_t tmem, int bh, int QB, int kk, cplx C, int k,
-                                             uint32_t &kph, const TileFetch &f, RowData rowdata)
+                                             uint32_t &kph, const TileFetch &f, RowData rowdata,
+                                             int withhold)
 {
     const int lane = threadIdx.x & 31, b = k & 1;
     const int KB = QB - kk;
@@ -207,7 +208,8 @@ __device__ __forceinline__ bool produce_tile(const OpArgs &a, const OpMaps &maps
     if (k >= 2 && !wait_bar_warp(m.sempty + b, ((k >> 1) + 1) & 1, m.abort, a.status, 0)) return false;
     const int kind = kk == 0 ? kTileDiag : ((GATED && !cnonzero(C)) ? kTileZero : kTileOff);
     unsigned char *st = m.base + L::stage + b * L::qk_bytes;
-    if (lane == 0 && kind != kTileZero) {
+    // test knob: block `withhold` loads nothing for its second tile, so the wait below runs out
+    if (lane == 0 && kind != kTileZero && !(k == 1 && (int)blockIdx.x == withhold)) {
         mbar_arrive_expect_tx(m.kfull + b, L::qk_bytes);
         for (int rr = 0; rr < DP / 64; ++rr) {
             tma_load_3d(st + rr * kRegion, &maps.q, m.kfull + b, rr * 64, QB * 128, bh);
@@ -378,7 +380,8 @@ operator_stats_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __g
             }
             if (GATED && cur.kk >= 1 && lane == 0)
                 a.ctab[((int64_t)cur.slot * nqt + cur.QB) * nqt + cur.QB - cur.kk] = make_float2(C.re, C.im);
-            ok = produce_tile<DP, GATED, L>(a, maps, m, tmem, bh, cur.QB, cur.kk, C, k, kph, fc, rowdata);
+            ok = produce_tile<DP, GATED, L>(a, maps, m, tmem, bh, cur.QB, cur.kk, C, k, kph, fc, rowdata,
+                                            a.withhold_stats);
             if (GATED && cur.kk >= 1) C = carry_step(C, {fc.ct.x, fc.ct.y});
         }
     } else {
@@ -488,9 +491,12 @@ operator_stats_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __g
 
 // ================================================================ row data
 
-// Per row of each query tile: the partials merged into (M, Z'), then the row factor
-// f = 2^{(1-beta) M} Z'^{-beta} (2^M at beta = 0) and f prefix_i for the write, and |prefix_i|
-// for its live test. One thread per row.
+// Per row of each query tile: the partials merged into (M, Z'), then the log2 of the row
+// factor, E = (1-beta) M - beta log2 Z' (M at beta = 0), and prefix_i for the write, and
+// |prefix_i| for its live test. One thread per row. The write forms each entry as
+// 2^{(t - M) + E} = 2^{t - beta log2 Z} in one exponential, so an entry is +-inf only where
+// its own value overflows (a row factor that overflows on its own never meets an entry that
+// underflows: no inf * 0).
 template <bool GATED>
 __global__ void __launch_bounds__(128)
 operator_rows_kernel(OpArgs a, const __grid_constant__ HeadTable tab)
@@ -515,8 +521,8 @@ operator_rows_kernel(OpArgs a, const __grid_constant__ HeadTable tab)
     float M = -INFINITY, Z = 0.f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) merge_stats(M, Z, pv[c].x, pv[c].y);
-    const float f = (beta == 0.f) ? exp2f(M) : exp2f((1.f - beta) * M - beta * log2f(Z));
-    a.rowf[base * 128 + r] = make_float4(M, f, pq.re * f, pq.im * f);
+    const float E = (beta == 0.f) ? M : (1.f - beta) * M - beta * log2f(Z);
+    a.rowf[base * 128 + r] = make_float4(M, E, pq.re, pq.im);
     a.rowq[base * 128 + r] = GATED ? cabs(pq) : pq.re;
     if (valid && (!isfinite(M) || !(Z > 0.f) || !isfinite(Z))) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
 }
@@ -581,7 +587,7 @@ operator_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __grid_co
             const int slot = tc / per_head, rem = tc - slot * per_head;
             const int QB = rem / nqt, kk = rem - QB * nqt;
             ok = produce_tile<DP, GATED, L>(a, maps, m, tmem, tab.bh[slot], QB, kk, {fc.ct.x, fc.ct.y}, k,
-                                            kph, fc, rowdata);
+                                            kph, fc, rowdata, a.withhold_write);
         }
     } else {
         const int q = warp & 3, h = warp >> 2;
@@ -674,8 +680,8 @@ operator_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __grid_co
                 put_zero(x0 + 32, y0, bh);
             } else {
                 const float scale2 = tab.qk[slot] * 1.4426950408889634f / sqrtf((float)a.d);
-                const float4 rs = m.rows[b * 128 + i];  // M, f, f prefix_i
-                const float M = rs.x;
+                const float4 rs = m.rows[b * 128 + i];  // M, E, prefix_i
+                const float M = rs.x, E = rs.y;
                 if (kind == kTileOff) {
                     const float rq = m.rq[b * 128 + i];
                     const bool fast = __all_sync(0xffffffffu, GATED ? rq * m.cmin[b] > 0.f : true);
@@ -688,16 +694,17 @@ operator_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __grid_co
                             const int j = 64 * h + 32 * cc + e;
                             const float tl = fminf(fmaf(sv[e], scale2, -M), 0.f);
                             if (GATED) {
-                                // W_ij = (f prefix_i) (C suffix_j) 2^{t - M}, in paired lanes
+                                // W_ij = (prefix_i) (C suffix_j) 2^{t - M + E}, in paired lanes;
+                                // a component of G that is exactly 0 stays 0 (no 0 * inf)
                                 const float4 c = m.col[b * 128 + j];
                                 const bool live = fast || rq * m.colm[b * 128 + j] > 0.f;
-                                const float p = live ? ex2_approx(tl) : 0.f;
-                                float2 w = fma2(fre, make_float2(c.x, c.y), mul2(fim, make_float2(c.z, c.w)));
-                                w = mul2(w, make_float2(p, p));
-                                vr[e] = w.x;
-                                vi[e] = w.y;
+                                const float p = live ? ex2_approx(tl + E) : 0.f;
+                                const float2 w = fma2(fre, make_float2(c.x, c.y), mul2(fim, make_float2(c.z, c.w)));
+                                const float2 wp = mul2(w, make_float2(p, p));
+                                vr[e] = w.x == 0.f ? 0.f : wp.x;
+                                vi[e] = w.y == 0.f ? 0.f : wp.y;
                             } else {
-                                vr[e] = rs.y * ex2_approx(tl);
+                                vr[e] = ex2_approx(tl + E);
                                 vi[e] = 0.f;
                             }
                         }
@@ -725,9 +732,9 @@ operator_kernel(OpArgs a, const __grid_constant__ HeadTable tab, const __grid_co
                                 R *= m.colm[b * 128 + j + 1];
                             }
                             const bool live = j <= i && R > 0.f;
-                            const float p = live ? rs.y * ex2_approx(fminf(fmaf(sv[e], scale2, -M), 0.f)) : 0.f;
-                            vr[e] = GATED ? G.re * p : p;
-                            vi[e] = GATED ? G.im * p : 0.f;
+                            const float p = live ? ex2_approx(fminf(fmaf(sv[e], scale2, -M), 0.f) + E) : 0.f;
+                            vr[e] = GATED ? (G.re == 0.f ? 0.f : G.re * p) : p;
+                            vi[e] = GATED ? (G.im == 0.f ? 0.f : G.im * p) : 0.f;
                         }
                         put(x0 + 32 * cc, y0, bh, vr, vi, !GATED);
                     }

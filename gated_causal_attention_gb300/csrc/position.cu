@@ -331,7 +331,9 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
         }
 
         // ------------------------------------------------------------ epilogue
-        // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0.
+        // O_i = e^{(1-beta) M} (sum_d kappa(d) v_{i-d}) / C(i)^beta; an exact 0 stays 0. The
+        // factor is applied as two equal halves f = e^{E/2}, O = (acc f) f, so that an output
+        // within fp32 is not lost to a factor that alone overflows or underflows.
         // Thread (h, r) works out the factor of row r of the lower (h = 0) or upper (h = 1) tile.
         {
             const int QA = h ? Qhi : Qlo;
@@ -342,7 +344,8 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
                 const float beta = tab.beta[slot], M = meta.x;
                 const float Ci = a.C[(int64_t)slot * n + row];
                 bad = !(Ci > 0.f);  // every kappa of the row underflowed
-                f = (beta == 0.f) ? expf(M) : expf((1.f - beta) * M - beta * logf(Ci));
+                const float E = (beta == 0.f) ? M : (1.f - beta) * M - beta * logf(Ci);
+                f = expf(0.5f * E);
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
             s_rowf[h * 128 + r] = f;
@@ -368,7 +371,7 @@ position_head_kernel(PosArgs a, const __grid_constant__ HeadTable tab, const __g
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const float x = __uint_as_float(acc[e]);
-                        st[(32 * qc + e) * DVP + d] = x == 0.f ? 0.f : x * rf[32 * qc + e];
+                        st[(32 * qc + e) * DVP + d] = x == 0.f ? 0.f : (x * rf[32 * qc + e]) * rf[32 * qc + e];
                     }
                 }
             }

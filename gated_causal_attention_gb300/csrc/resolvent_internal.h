@@ -91,6 +91,7 @@ struct HeadArgs {
     int tma_out;  // O staged in shared memory and written by coalesced 16-byte stores (dv % 4 == 0); else plain stores
     int heads_per_group;  // blocks are ordered head group by head group (1 <= it <= table count)
     int *numkv;           // [slots * nqt] off-diagonal key tiles of each query tile (gated heads)
+    int withhold;         // test knob: this block's K/V loads stop after its first tile (-1: none)
 };
 // The tensor maps of one head launch: q, k, v (bf16, box 64 x 128).
 struct HeadMaps {
@@ -115,6 +116,8 @@ struct OpArgs {
     float *rowq;                 // [slots, nqt * 128] |prefix_i| (1 ungated; 0 past n)
     int32_t *status;
     int tma_out;                 // W written by tensor-map stores (n % 4 == 0); else plain stores
+    int withhold_stats;          // test knobs: this block of the statistics / write launch loads
+    int withhold_write;          //   nothing for its second tile (-1: none)
 };
 // q, k (bf16, box 64 x 128) and, when tma_out is set, W_re and W_im (fp32, box 32 x 32).
 struct OpMaps {

@@ -210,13 +210,18 @@ rs_status resolvent_chain_scan_carry(const float *u, const float *theta, rs_swit
  * Limit: the sizes must need at most 8 MiB of chain scratch, i.e.
  * resolvent_chain_workspace_bytes(B, H, n, dv) <= 8 MiB (about 1M tokens of B*H*n per 128
  * heads at dv = 64); larger calls return RS_ERR_UNSUPPORTED and launch nothing.
- * The array is reserved on every GPU that loads the library and held until the process
- * exits. The first call on a device looks up the array's device address (one
- * cudaGetSymbolAddress with that device current); make that first call before any stream
- * capture. Nothing is allocated or freed, by this library or any library it calls. The
- * counters that must start at zero are cleared on the stream at the start of every call;
- * the rest keeps the last call's contents. All calls share the one array, so calls that
- * overlap on the GPU (other streams, other threads) race: serialise them.
+ * The array is part of this library's device code: it is reserved in a device's memory when
+ * that code is loaded there and held until the process exits. Under CUDA's lazy module
+ * loading (the default) that happens at the first call on the device that needs it, so in a
+ * process whose memory pool will take all device memory, make the first call of this entry
+ * point before the pool does, or the load can fail (RS_ERR_CUDA). The first
+ * call on a device also looks up the array's device address (one cudaGetSymbolAddress with
+ * that device current); make it before any stream capture. The address is kept per device
+ * and context, and looked up again in a new context (after cudaDeviceReset).
+ * Nothing is allocated or freed, by this library or any library it calls. The counters that
+ * must start at zero are cleared on the stream at the start of every call; the rest keeps
+ * the last call's contents. All calls share the one array, so calls that overlap on the GPU
+ * (other streams, other threads) race: serialise them.
  * Arguments, layout, errors and results are those of resolvent_chain_scan.
  */
 rs_status resolvent_chain_scan_noalloc(const float *u, const float *theta, rs_switches sw,
@@ -225,7 +230,8 @@ rs_status resolvent_chain_scan_noalloc(const float *u, const float *theta, rs_sw
                                        int32_t *status_dev, void *stream);
 
 /* Synchronises `stream`, reads the status word, clears it to 0 and returns RS_OK,
- * RS_ERR_NONFINITE or RS_ERR_TIMEOUT (RS_ERR_CUDA if the runtime reports an error). */
+ * RS_ERR_TIMEOUT or RS_ERR_NONFINITE (RS_ERR_CUDA if the runtime reports an error). A timeout
+ * takes precedence: after one the outputs, and any refusal raised from them, are unspecified. */
 rs_status resolvent_status_sync(int32_t *status_dev, void *stream);
 
 /* Static text for a status code. */
@@ -252,21 +258,38 @@ rs_status resolvent_debug_path_product(const float *u, const float *theta, rs_sw
  *  - a block of the position-head kernel whose V loads stop after its first (-1: none): its
  *    tensor-core issuer's wait for the next V tile runs out (2 s), RS_STATUS_TIMEOUT is
  *    raised, every block winds down (each waits for the copies and products it started) and
- *    the call returns.
+ *    the call returns;
+ *  - the same for a block of the fused head kernel, whose K and V loads stop after its first
+ *    key tile (-1: none);
+ *  - the same for a block of the operator's statistics launch (launch 0) or write launch
+ *    (launch 1), which loads nothing for its second tile (block -1: none).
  */
 void resolvent_test_set_wait_limit_ns(uint64_t ns);
 void resolvent_test_set_chain_withhold(int ticket);
 void resolvent_test_set_position_withhold(int block);
+void resolvent_test_set_head_withhold(int block);
+void resolvent_test_set_operator_withhold(int launch, int block);
 
 /*
- * Kernel timing (benchmarking): while enabled, each call records a pair of CUDA events on
- * its stream around its main kernel -- the fused head kernel(s), or the chain scan when the
- * call has no other heads. resolvent_profile_collect waits for the recorded pairs, writes
- * their durations in milliseconds (at most `max`), returns how many, and starts a new
- * series (-1 on a CUDA error). Enabling (re)starts the series. Up to 1024 pairs are kept.
+ * Kernel timing (benchmarking): while enabled, each call records pairs of CUDA events on its
+ * stream around its main launches, one pair per class below: each table of gated heads
+ * (the key-tile count and the fused head kernel), each table of g = 0 heads, the O(n)
+ * readout of qk = 0 heads, the chain scan, the operator's write of W, the position heads
+ * (prep and main launch), gate preparation. resolvent_profile_collect waits for the
+ * recorded pairs, writes their durations in milliseconds (at most `max`), returns how many,
+ * and starts a new series (-1 on a CUDA error); resolvent_profile_collect_kinds also writes
+ * each pair's class. Enabling (re)starts the series. Up to 4096 pairs are kept.
  */
+#define RS_PROF_HEAD_GATED 0
+#define RS_PROF_HEAD_REAL 1
+#define RS_PROF_READOUT 2
+#define RS_PROF_CHAIN 3
+#define RS_PROF_OPERATOR 4
+#define RS_PROF_POSITION 5
+#define RS_PROF_GATE_PREP 6
 rs_status resolvent_profile_enable(int on);
 int resolvent_profile_collect(float *ms, int max);
+int resolvent_profile_collect_kinds(float *ms, int *kind, int max);
 
 #ifdef __cplusplus
 }
