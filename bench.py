@@ -2,14 +2,19 @@
 """Benchmark of the resolvent-operator causal head on GB300.
 
 A step is one call of the hot path on one batch of seeded synthetic inputs already resident
-in HBM: resolvent_head_forward (gate preparation + fused head kernel, and the chain scan for
-heads at qk = 0, beta = 0) for the head workloads, resolvent_chain_scan for the chain
-workload. The default workload is the gated softmax head (B=8 H=16 n=2048 d=dv=64 bf16,
-(beta, qk, g) = (1, 1, 0.5)).
+in HBM: resolvent_head_forward (gate preparation, the fused head kernel for heads with
+qk != 0, the O(n) readout for heads with qk = 0) for the head workloads, resolvent_chain_scan
+for the chain, resolvent_operator, resolvent_position_head, resolvent_gate_prep. The
+default workload is the largest single-GPU configuration, the mixed-switch heads (B=1 H=64
+n=32768 d=dv=128 bf16, every dispatch class: gated and g = 0 heads on the fused kernel, qk = 0
+heads on the O(n) readout).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle instead, on the
+Prints one JSON line (rank 0): the throughput, the roofline of the dominant kernel, per-class
+figures (mixed heads), the fp64 oracle on the host cores (cpu_baseline), the same metric end
+to end from pinned host memory through the overlapped host pipeline (e2e), and the SM clocks
+sampled during the timed region. `--impl reference` times the fp64 CPU oracle instead, on the
 host cores, with a bounded sample of the same workload per step.
 Multi-GPU (torchrun): every rank runs its own full batch (independent heads, no collective
 on the data path): weak scaling; the time is the max over ranks.
@@ -40,7 +45,7 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default="gated_softmax", choices=sorted(W.WORKLOADS))
+    p.add_argument("--workload", default="mixed", choices=sorted(W.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample (cpu_baseline and --impl reference)")
@@ -111,16 +116,32 @@ def head_work(hi: W.HeadInputs):
     """Algorithmic flops of the fused head kernel(s) for one call: per head with qk != 0,
     live entries x (2 d + 2 dv c), c = 2 with complex gates (g != 0), else 1. Heads with
     qk = 0 run as O(n) chains (O_i = y_i Z_i^-beta) and count as chain tokens."""
+    c = head_classes(hi)
+    return c["gated_flops"] + c["real_flops"], c["chain_tokens"]
+
+
+def head_classes(hi: W.HeadInputs):
+    """Per dispatch class of a head workload: the fused kernel's gated heads (g != 0) and real
+    heads (g = 0) with their algorithmic flops and entry counts, and the qk = 0 heads that run
+    as O(n) readouts."""
     beta, qk, g = hi.switches_bh()
-    flops, chain_tokens = 0.0, 0
+    out = {"gated_heads": 0, "gated_flops": 0.0, "gated_live": 0.0, "gated_causal": 0.0,
+           "real_heads": 0, "real_flops": 0.0, "chain_heads": 0, "chain_tokens": 0}
+    causal = hi.n * (hi.n + 1) / 2
     for h in range(hi.B * hi.H):
         if qk[h] == 0.0:
-            chain_tokens += hi.n
-            continue
-        per_entry = 2 * hi.d + 2 * hi.dv * (2 if g[h] != 0.0 else 1)
-        flops += per_entry * (live_entries(hi.u[h], g[h]) if g[h] != 0.0
-                              else hi.n * (hi.n + 1) / 2)
-    return flops, chain_tokens
+            out["chain_heads"] += 1
+            out["chain_tokens"] += hi.n
+        elif g[h] != 0.0:
+            live = live_entries(hi.u[h], g[h])
+            out["gated_heads"] += 1
+            out["gated_live"] += live
+            out["gated_causal"] += causal
+            out["gated_flops"] += live * (2 * hi.d + 4 * hi.dv)
+        else:
+            out["real_heads"] += 1
+            out["real_flops"] += causal * (2 * hi.d + 2 * hi.dv)
+    return out
 
 
 def position_work(pi: W.PositionInputs):
@@ -143,7 +164,78 @@ def chain_bytes_per_token(dv, b_bytes=4):
 
 # ------------------------------------------------------------------ clocks
 
-class Clocks:
+class NvmlClocks:
+    """SM clock, throttle reasons and power sampled every ~2 ms from NVML (read only) in a
+    thread, so that the timed region itself is covered."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+        import torch
+        self.ct = ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            cnt = ctypes.c_uint(0)
+            L.nvmlDeviceGetCount_v2(ctypes.byref(cnt))
+            idx = 0 if cnt.value == 1 else torch.device(device).index or 0
+            if L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        self.L, self.h = L, h
+        self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        ct = self.ct
+        clk, rs, pw = ct.c_uint(0), ct.c_ulonglong(0), ct.c_uint(0)
+        self.L.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk))
+        self.reasons_fn(self.h, ct.byref(rs))
+        self.L.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        self.samples.append((time.perf_counter(), float(clk.value), int(rs.value), pw.value / 1e3))
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            self._sample()
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self, t0, t1):
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        use = inside if inside else self.samples
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"]}
+        bits = 0
+        for x in use:
+            bits |= x[2]
+        return {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(v for b, v in self.REASONS.items() if bits & b),
+                "power_w_max": max(x[3] for x in use), "samples": len(use),
+                "samples_in_timed_region": len(inside), "source": "nvml, every ~2 ms"}
+
+
+class SmiClocks:
+    """Fallback: nvidia-smi sampling every 100 ms (too coarse for short timed regions)."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -165,8 +257,6 @@ class Clocks:
             self.proc = None
 
     def stop(self, t0, t1):
-        """Summary of the samples taken in [t0, t1] (wall clock), widened to the whole
-        sampling window when fewer than 3 samples fall inside."""
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -194,13 +284,22 @@ class Clocks:
         reasons = sorted({names[i] for r in use for i, v in enumerate(r[3][1:5])
                           if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "source": "nvidia-smi, every 100 ms"}
+
+
+def make_clocks(device, local):
+    try:
+        return NvmlClocks(device)
+    except Exception:
+        return SmiClocks(local)
 
 
 KERNEL_SOURCES = {"head_fwd_kernel": ["head_fwd.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"],
                   "chain_scan_kernel": ["chain_scan.cu", "common.cuh"],
                   "operator_kernel": ["operator.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"],
-                  "position_head_kernel": ["position.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"]}
+                  "position_head_kernel": ["position.cu", "head_common.cuh", "common.cuh", "gate_products.cuh"],
+                  "gate_prep_kernel": ["gate_prep.cu", "gate_products.cuh", "common.cuh"]}
 
 
 def measured_traffic(kernel, workload):
@@ -298,10 +397,40 @@ def oracle_sample_position(pi: W.PositionInputs, target_s: float):
     return heads * pi.n / dt, heads * pi.n, dt
 
 
+def oracle_sample_gate(gi: W.GateInputs, target_s: float):
+    """The oracle's gate preparation (blend, gate, block products) of whole heads."""
+    import oracle
+    oracle.build()
+    g = np.asarray(gi.switches_bh()[2], np.float32).astype(np.float64)
+    heads, t0 = 0, time.perf_counter()
+    while heads < gi.B * gi.H and (heads == 0 or time.perf_counter() - t0 < target_s):
+        oracle.gate_prep(gi.u[heads:heads + 1], gi.theta[heads:heads + 1], g[heads:heads + 1])
+        heads += 1
+    dt = time.perf_counter() - t0
+    return heads * gi.n / dt, heads * gi.n, dt
+
+
 def cpu_cores():
     import oracle
     oracle.build()
     return oracle.max_threads()
+
+
+def kind_of(inp, workload):
+    if isinstance(inp, W.ChainInputs):
+        return "chain"
+    if isinstance(inp, W.PositionInputs):
+        return "position"
+    if isinstance(inp, W.GateInputs):
+        return "gate_prep"
+    return "operator" if workload == "operator" else "head"
+
+
+METRICS = {"chain": ("chain tokens/s (B*H*n/s)", "tokens/s"),
+           "position": ("position tokens/s (B*H*n/s)", "tokens/s"),
+           "gate_prep": ("gate-prep tokens/s (B*H*n/s)", "tokens/s"),
+           "operator": ("operator entries/s (B*H*n*n/s)", "entries/s"),
+           "head": ("head tokens/s (B*H*n/s)", "tokens/s")}
 
 
 def config_of(args, inp, world):
@@ -313,6 +442,10 @@ def config_of(args, inp, world):
         cfg = {"workload": args.workload, "B": inp.B, "H": inp.H, "n": inp.n, "dv": inp.dv,
                "dtype_v": inp.dtype, "logits": "a_h(d) = -2^(-8(h+1)/H) d + 0.5 N(0,1)",
                "switches (beta, qk; g = 0)": sw[0] if len(sw) == 1 else f"{len(sw)} per-head settings"}
+    elif isinstance(inp, W.GateInputs):
+        cfg = {"workload": args.workload, "B": inp.B, "H": inp.H, "n": inp.n,
+               "inputs": "u ~ U(-0.5,1.5), theta ~ U(-pi,pi) fp32", "g": "per head, grid {0, 0.3, 1}",
+               "outputs": "m, theta', gate, prefix, suffix, block carries"}
     else:
         sw = sorted({(float(b), float(q), float(g)) for b, q, g in zip(inp.beta, inp.qk, inp.g)})
         cfg = {"workload": args.workload, "B": inp.B, "H": inp.H, "n": inp.n, "d": inp.d,
@@ -330,17 +463,13 @@ def run_reference(args):
         return
     inp = make_inputs(args)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup) * 2)
-    is_chain = isinstance(inp, W.ChainInputs)
-    is_op = args.workload == "operator"
-    is_pos = isinstance(inp, W.PositionInputs)
-    if is_chain:
-        sample = lambda: oracle_sample_chain(inp, per_step)
-    elif is_pos:
-        sample = lambda: oracle_sample_position(inp, per_step)
-    elif is_op:
-        sample = lambda: oracle_sample_operator(inp, per_step)
-    else:
-        sample = lambda: oracle_sample_head(inp, per_step, seed=7)
+    kind = kind_of(inp, args.workload)
+    is_op = kind == "operator"
+    sample = {"chain": lambda: oracle_sample_chain(inp, per_step),
+              "position": lambda: oracle_sample_position(inp, per_step),
+              "operator": lambda: oracle_sample_operator(inp, per_step),
+              "gate_prep": lambda: oracle_sample_gate(inp, per_step),
+              "head": lambda: oracle_sample_head(inp, per_step, seed=7)}[kind]
     for _ in range(args.warmup):
         sample()
     rates, toks, secs = [], 0, 0.0
@@ -351,20 +480,18 @@ def run_reference(args):
         secs += s
     value = toks / secs
     cores = cpu_cores()
-    unit = "entries/s" if is_op else "tokens/s"
-    metric = ("chain tokens/s (B*H*n/s)" if is_chain else
-              "operator entries/s (B*H*n*n/s)" if is_op else
-              "position tokens/s (B*H*n/s)" if is_pos else "head tokens/s (B*H*n/s)")
+    metric, unit = METRICS[kind]
     line = {"impl": "reference", "metric": metric,
             "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, workloads.py)", "config": config_of(args, inp, 1),
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
-                             "sample": ("whole heads of the chain" if is_chain else
-                                        "whole heads' W" if is_op else
-                                        "whole position-only heads" if is_pos else
-                                        "seeded random rows of every head") +
+                             "sample": {"chain": "whole heads of the chain",
+                                        "operator": "whole heads' W",
+                                        "position": "whole position-only heads",
+                                        "gate_prep": "whole heads' gate preparation",
+                                        "head": "seeded random rows of every head"}[kind] +
                              f", {toks} {'entries' if is_op else 'tokens'} in {secs:.1f} s"},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -372,6 +499,165 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+
+def setup_workload(args, inp, device, R):
+    """The device-resident step, its work accounting and its end-to-end description."""
+    import torch
+    kind = kind_of(inp, args.workload)
+    shp = (inp.B, inp.H, inp.n)
+    tdev = lambda x, s, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(
+        device=device, dtype=dt)
+    status = R.new_status(device)
+    w = {"kind": kind, "status": status}
+    if kind == "chain":
+        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
+        b = tdev(inp.b, (*shp, inp.dv))
+        ws = torch.empty(max(1, R.chain_workspace_bytes(*shp, inp.dv)), dtype=torch.uint8, device=device)
+
+        def call(di, do, stream=None):
+            R.chain_scan(di[0], di[1], inp.g, di[2], out=(do[0], do[1]), workspace=ws, status=status,
+                         stream=stream, sync=False)
+        dev_in = [u, th, b]
+        dev_out = [torch.empty_like(b), torch.empty_like(b)]
+        host_in = [(inp.u, shp, torch.float32), (inp.theta, shp, torch.float32),
+                   (inp.b, (*shp, inp.dv), torch.float32)]
+        w.update(tokens=inp.B * inp.H * inp.n, main=[R.PROF_CHAIN], bound="hbm",
+                 kname="chain_scan_kernel", dtype="f32",
+                 work=inp.B * inp.H * inp.n * chain_bytes_per_token(inp.dv))
+    elif kind == "operator":
+        q, k = tdev(inp.q, (*shp, inp.d), torch.bfloat16), tdev(inp.k, (*shp, inp.d), torch.bfloat16)
+        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
+        ws = torch.empty(max(1, R.operator_workspace_bytes(*shp, inp.d, torch.bfloat16)),
+                         dtype=torch.uint8, device=device)
+
+        def call(di, do, stream=None):
+            R.operator(di[0], di[1], di[2], di[3], inp.beta, inp.qk, inp.g, out=(do[0], do[1]),
+                       workspace=ws, status=status, stream=stream, sync=False)
+        dev_in = [q, k, u, th]
+        dev_out = [torch.empty(*shp, inp.n, device=device), torch.empty(*shp, inp.n, device=device)]
+        host_in = [(inp.q, (*shp, inp.d), torch.bfloat16), (inp.k, (*shp, inp.d), torch.bfloat16),
+                   (inp.u, shp, torch.float32), (inp.theta, shp, torch.float32)]
+        entries = inp.B * inp.H * inp.n * inp.n
+        # bytes: W written (8 B per entry); q, k read (2 B x d each per token); u, theta
+        w.update(tokens=entries, main=[R.PROF_OPERATOR], bound="hbm", kname="operator_kernel",
+                 dtype="f32", work=entries * 8 + inp.B * inp.H * inp.n * (4 * inp.d + 8))
+    elif kind == "position":
+        a = tdev(inp.a, (inp.H, inp.n))
+        v = tdev(inp.v, (*shp, inp.dv), torch.bfloat16)
+        ws = torch.empty(max(1, R.position_workspace_bytes(*shp, inp.dv, torch.bfloat16)),
+                         dtype=torch.uint8, device=device)
+
+        def call(di, do, stream=None):
+            R.position_head(di[0], di[1], inp.beta, inp.qk, out=do[0], workspace=ws, status=status,
+                            stream=stream, sync=False)
+        dev_in = [a, v]
+        dev_out = [torch.empty(*shp, inp.dv, device=device)]
+        host_in = [(inp.a, (inp.H, inp.n), torch.float32), (inp.v, (*shp, inp.dv), torch.bfloat16)]
+        w.update(tokens=inp.B * inp.H * inp.n, main=[R.PROF_POSITION], bound="tensor",
+                 kname="position_head_kernel", dtype="bf16", work=position_work(inp))
+    elif kind == "gate_prep":
+        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
+        outs = R.gate_prep_outputs(*shp, device)
+        names = ["m", "theta_p", "gate", "prefix", "suffix", "carry"]
+
+        def call(di, do, stream=None):
+            R.gate_prep(di[0], di[1], inp.g, out=dict(zip(names, do)), status=status, stream=stream,
+                        sync=False)
+        dev_in = [u, th]
+        dev_out = [outs[k] for k in names]
+        host_in = [(inp.u, shp, torch.float32), (inp.theta, shp, torch.float32)]
+        nb = (inp.n + 127) // 128
+        tokens = inp.B * inp.H * inp.n
+        # u, theta read; m, theta' (4 B each) and gate, prefix, suffix (8 B each) written; carries
+        w.update(tokens=tokens, main=[R.PROF_GATE_PREP], bound="hbm", kname="gate_prep_kernel",
+                 dtype="f32", work=tokens * (8 + 32) + inp.B * inp.H * nb * 8)
+    else:
+        dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+        q, k = tdev(inp.q, (*shp, inp.d), dt), tdev(inp.k, (*shp, inp.d), dt)
+        v = tdev(inp.v, (*shp, inp.dv), dt)
+        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
+        ws = torch.empty(max(1, R.head_workspace_bytes(*shp, inp.d, inp.dv, dt)), dtype=torch.uint8,
+                         device=device)
+
+        def call(di, do, stream=None):
+            R.head_forward(di[0], di[1], di[2], di[3], di[4], inp.beta, inp.qk, inp.g,
+                           out=(do[0], do[1]), workspace=ws, status=status, stream=stream, sync=False)
+        dev_in = [q, k, u, th, v]
+        dev_out = [torch.empty(*shp, inp.dv, device=device), torch.empty(*shp, inp.dv, device=device)]
+        host_in = [(inp.q, (*shp, inp.d), dt), (inp.k, (*shp, inp.d), dt), (inp.u, shp, torch.float32),
+                   (inp.theta, shp, torch.float32), (inp.v, (*shp, inp.dv), dt)]
+        cls = head_classes(inp)
+        w.update(tokens=inp.B * inp.H * inp.n, main=[R.PROF_HEAD_GATED, R.PROF_HEAD_REAL],
+                 bound="tensor", kname="head_fwd_kernel",
+                 dtype="bf16" if inp.dtype == "bf16" else "f32->bf16",
+                 work=cls["gated_flops"] + cls["real_flops"], classes=cls)
+    w.update(call=call, dev_in=dev_in, dev_out=dev_out, host_in=host_in,
+             step=lambda: call(dev_in, dev_out))
+    return w
+
+
+def class_figures(w, inp, per_kind_ms, pk):
+    """Per dispatch class of a head workload: time per step, throughput and roofline fraction
+    of the gated and real fused-kernel launches and of the O(n) readout of qk = 0 heads."""
+    import gated_causal_attention_gb300 as R
+    c = w.get("classes")
+    if not c:
+        return None
+    out = {}
+    t = per_kind_ms.get(R.PROF_HEAD_GATED, 0.0)
+    if c["gated_heads"]:
+        tf = c["gated_flops"] / (t / 1e3) / 1e12 if t > 0 else None
+        out["k2_gated"] = {"heads": c["gated_heads"], "ms": t, "tflops": tf,
+                           "frac": tf / pk["bf16_tflops"] if tf else None,
+                           "skip_fraction": 1.0 - c["gated_live"] / c["gated_causal"]}
+    t = per_kind_ms.get(R.PROF_HEAD_REAL, 0.0)
+    if c["real_heads"]:
+        tf = c["real_flops"] / (t / 1e3) / 1e12 if t > 0 else None
+        out["k2_real"] = {"heads": c["real_heads"], "ms": t, "tflops": tf,
+                          "frac": tf / pk["bf16_tflops"] if tf else None}
+    t = per_kind_ms.get(R.PROF_READOUT, 0.0)
+    if c["chain_heads"]:
+        vb = 2 if inp.dtype == "bf16" else 4
+        byt = c["chain_tokens"] * (vb * inp.dv + 8 + 8 * inp.dv)
+        gbs = byt / (t / 1e3) / 1e9 if t > 0 else None
+        out["qk0_readout"] = {"heads": c["chain_heads"], "ms": t, "gbs": gbs,
+                              "frac": gbs / pk["hbm_gbs"] if gbs else None,
+                              "bytes_per_token": vb * inp.dv + 8 + 8 * inp.dv}
+    return out
+
+
+def run_e2e(args, w, device, world, R):
+    """The same metric end to end: every step uploads its inputs from pinned host memory, runs
+    the call and reads its outputs back to pinned host memory, through the overlapped host
+    pipeline (uploads, calls, downloads on three streams, double-buffered device memory)."""
+    import torch
+    from gated_causal_attention_gb300.pipeline import HostPipeline
+    pinned = [torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(dt).pin_memory()
+              for x, s, dt in w["host_in"]]
+    specs_in = [(tuple(p.shape), p.dtype) for p in pinned]
+    specs_out = [(tuple(o.shape), o.dtype) for o in w["dev_out"]]
+    pipe = HostPipeline(lambda di, do, st: w["call"](di, do, st), specs_in, specs_out, device=device)
+    host_out = [[torch.empty(s, dtype=dt).pin_memory() for s, dt in specs_out] for _ in range(2)]
+    h2d = sum(p.numel() * p.element_size() for p in pinned)
+    d2h = sum(o.numel() * o.element_size() for o in host_out[0])
+    for i in range(3):
+        pipe.submit(pinned, host_out[i % 2])
+    pipe.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(pipe.up)
+    for i in range(args.steps):
+        pipe.submit(pinned, host_out[i % 2])
+    e1.record(pipe.down)
+    pipe.synchronize()
+    e_ms = dist_max(e0.elapsed_time(e1) / args.steps, world, device)
+    R.status_sync(w["status"])
+    unit = METRICS[w["kind"]][1]
+    return {"value": w["tokens"] * world / (e_ms / 1e3), "unit": unit, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+            "how": "pinned host buffers; uploads, calls and downloads overlapped on three streams"}
+
 
 def run_ours(args):
     import torch
@@ -385,194 +671,86 @@ def run_ours(args):
     __graft_entry__.build()
 
     inp = make_inputs(args)
-    is_chain = isinstance(inp, W.ChainInputs)
-    is_op = args.workload == "operator"
-    is_pos = isinstance(inp, W.PositionInputs)
-    shp = (inp.B, inp.H, inp.n)
-    tdev = lambda x, s, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(
-        device=device, dtype=dt)
-    status = R.new_status(device)
-    if is_chain:
-        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
-        b = tdev(inp.b, (*shp, inp.dv))
-        out = (torch.empty_like(b), torch.empty_like(b))
-        ws = torch.empty(max(1, R.chain_workspace_bytes(*shp, inp.dv)), dtype=torch.uint8, device=device)
-        step = lambda: R.chain_scan(u, th, inp.g, b, out=out, workspace=ws, status=status, sync=False)
-        tokens = inp.B * inp.H * inp.n
-        work = tokens * chain_bytes_per_token(inp.dv)
-        host_in = [inp.u, inp.theta, inp.b]
-    elif is_op:
-        q, k = tdev(inp.q, (*shp, inp.d), torch.bfloat16), tdev(inp.k, (*shp, inp.d), torch.bfloat16)
-        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
-        out = (torch.empty(*shp, inp.n, device=device), torch.empty(*shp, inp.n, device=device))
-        ws = torch.empty(max(1, R.operator_workspace_bytes(*shp, inp.d, torch.bfloat16)),
-                         dtype=torch.uint8, device=device)
-        step = lambda: R.operator(q, k, u, th, inp.beta, inp.qk, inp.g, out=out, workspace=ws,
-                                  status=status, sync=False)
-        tokens = inp.B * inp.H * inp.n * inp.n  # entries of W
-        # bytes: W written (8 B per entry); q, k read (2 B x d each per token); u, theta
-        work = tokens * 8 + inp.B * inp.H * inp.n * (4 * inp.d + 8)
-        host_in = [inp.q, inp.k, inp.u, inp.theta]
-    elif is_pos:
-        a = tdev(inp.a, (inp.H, inp.n))
-        v = tdev(inp.v, (*shp, inp.dv), torch.bfloat16)
-        out = torch.empty(*shp, inp.dv, device=device)
-        ws = torch.empty(max(1, R.position_workspace_bytes(*shp, inp.dv, torch.bfloat16)),
-                         dtype=torch.uint8, device=device)
-        step = lambda: R.position_head(a, v, inp.beta, inp.qk, out=out, workspace=ws, status=status,
-                                       sync=False)
-        tokens = inp.B * inp.H * inp.n
-        work = position_work(inp)
-        host_in = [inp.a, inp.v]
-    else:
-        dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
-        q, k = tdev(inp.q, (*shp, inp.d), dt), tdev(inp.k, (*shp, inp.d), dt)
-        v = tdev(inp.v, (*shp, inp.dv), dt)
-        u, th = tdev(inp.u, shp), tdev(inp.theta, shp)
-        out = (torch.empty(*shp, inp.dv, device=device), torch.empty(*shp, inp.dv, device=device))
-        ws = torch.empty(max(1, R.head_workspace_bytes(*shp, inp.d, inp.dv, dt)), dtype=torch.uint8,
-                         device=device)
-        step = lambda: R.head_forward(q, k, u, th, v, inp.beta, inp.qk, inp.g, out=out, workspace=ws,
-                                      status=status, sync=False)
-        tokens = inp.B * inp.H * inp.n
-        work, chain_tokens = head_work(inp)
-        host_in = [inp.q, inp.k, inp.v, inp.u, inp.theta]
+    w = setup_workload(args, inp, device, R)
+    step = w["step"]
 
     # warm-up, and a refusal check of the inputs
     for _ in range(args.warmup):
         step()
-    R.status_sync(status)
+    R.status_sync(w["status"])
     launches_per_step = R.last_launch_count()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
 
-    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                    else local)
+    clocks = make_clocks(device, local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.05)
     R.profile_enable(True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     dist_barrier(world)
     torch.cuda.synchronize()
-    w0 = time.time()
+    w0 = time.perf_counter() if isinstance(clocks, NvmlClocks) else time.time()
     for i in range(args.steps):
         flush.zero_()  # L2 flush between timed iterations (outside the step's events)
         ev[i][0].record()
         step()
         ev[i][1].record()
     torch.cuda.synchronize()
+    w1 = time.perf_counter() if isinstance(clocks, NvmlClocks) else time.time()
     dist_barrier(world)
-    w1 = time.time()
-    kernel_ms = R.profile_collect()
+    pairs = R.profile_collect(kinds=True)
     R.profile_enable(False)
-    R.status_sync(status)
+    R.status_sync(w["status"])
     clk = clocks.stop(w0, w1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = sum(step_ms) / len(step_ms)
     ms = dist_max(ms_local, world, device)
-    value = tokens * world / (ms / 1e3)
+    value = w["tokens"] * world / (ms / 1e3)
 
+    per_kind = {}
+    for t, kd in pairs:
+        per_kind[kd] = per_kind.get(kd, 0.0) + t / args.steps
+    kern = sum(per_kind.get(kd, 0.0) for kd in w["main"]) or float("nan")
     pk, pk_kind = peaks()
-    kern = statistics.mean(kernel_ms) if kernel_ms else float("nan")
-    if is_chain or is_op:
-        kname = "chain_scan_kernel" if is_chain else "operator_kernel"
-        achieved = work / (kern / 1e3) / 1e9
+    if w["bound"] == "hbm":
+        achieved = w["work"] / (kern / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"],
-                "traffic": measured_traffic(kname, args.workload), "kernel": kname,
-                "kernel_ms": kern, "peak_kind": pk_kind,
-                "algorithmic_bytes_per_launch": work}
+                "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes_per_launch": w["work"]}
     else:
-        kname = "position_head_kernel" if is_pos else "head_fwd_kernel"
-        achieved = work / (kern / 1e3) / 1e12
+        achieved = w["work"] / (kern / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"],
-                "traffic": measured_traffic(kname, args.workload), "kernel": kname,
-                "kernel_ms": kern, "peak_kind": pk_kind + " burst",
-                "algorithmic_flops_per_launch": work}
+                "frac": achieved / pk["bf16_tflops"], "algorithmic_flops_per_launch": w["work"]}
+    roof.update(traffic=measured_traffic(w["kname"], args.workload), kernel=w["kname"],
+                kernel_ms=kern, peak_kind=pk_kind + (" burst" if w["bound"] == "tensor" else " copy"))
+    classes = class_figures(w, inp, per_kind, pk)
 
-    # end to end through the public API, pinned host buffers in and out
-    e2e = None
-    if not args.no_e2e:
-        pinned = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in host_in]
-        if is_op:
-            pinned[0] = pinned[0].to(torch.bfloat16).pin_memory()
-            pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
-        elif is_pos:
-            pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
-        elif not is_chain and inp.dtype == "bf16":
-            pinned[0] = pinned[0].to(torch.bfloat16).pin_memory()
-            pinned[1] = pinned[1].to(torch.bfloat16).pin_memory()
-            pinned[2] = pinned[2].to(torch.bfloat16).pin_memory()
-        outs_host = [torch.empty((out if is_pos else out[0]).shape, dtype=torch.float32).pin_memory()
-                     for _ in range(1 if is_pos else 2)]
-        h2d = sum(p.numel() * p.element_size() for p in pinned)
-        d2h = sum(o.numel() * o.element_size() for o in outs_host)
-
-        def e2e_step():
-            dv_in = [p.to(device, non_blocking=True) for p in pinned]
-            if is_chain:
-                uu, tt, bb = dv_in
-                o = R.chain_scan(uu.view(shp), tt.view(shp), inp.g, bb.view(*shp, inp.dv), out=out,
-                                 workspace=ws, status=status, sync=False)
-            elif is_op:
-                qq, kk, uu, tt = dv_in
-                o = R.operator(qq.view(*shp, inp.d), kk.view(*shp, inp.d), uu.view(shp),
-                               tt.view(shp), inp.beta, inp.qk, inp.g, out=out, workspace=ws,
-                               status=status, sync=False)
-            elif is_pos:
-                aa, vv = dv_in
-                o = (R.position_head(aa.view(inp.H, inp.n), vv.view(*shp, inp.dv), inp.beta, inp.qk,
-                                     out=out, workspace=ws, status=status, sync=False),)
-            else:
-                qq, kk, vv, uu, tt = dv_in
-                o = R.head_forward(qq.view(*shp, inp.d), kk.view(*shp, inp.d), uu.view(shp),
-                                   tt.view(shp), vv.view(*shp, inp.dv), inp.beta, inp.qk, inp.g,
-                                   out=out, workspace=ws, status=status, sync=False)
-            for oh, od in zip(outs_host, o):
-                oh.copy_(od, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        dist_barrier(world)
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.steps):
-            e2e_step()
-        b2.record()
-        torch.cuda.synchronize()
-        e_ms = dist_max(a.elapsed_time(b2) / args.steps, world, device)
-        R.status_sync(status)
-        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "entries/s" if is_op else "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+    e2e = None if args.no_e2e else run_e2e(args, w, device, world, R)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, toks, secs = (oracle_sample_chain(inp, args.cpu_seconds) if is_chain
-                            else oracle_sample_operator(inp, args.cpu_seconds) if is_op
-                            else oracle_sample_position(inp, args.cpu_seconds) if is_pos
-                            else oracle_sample_head(inp, args.cpu_seconds))
-        cpu = {"value": rate, "unit": "entries/s" if is_op else "tokens/s", "cores": cpu_cores(),
-               "kind": "oracle",
-               "sample": (f"{toks // inp.n} whole heads" if is_chain or is_pos else
-                          f"{toks // (inp.n * inp.n)} whole heads' W" if is_op else
-                          f"{toks // (inp.B * inp.H)} seeded random rows of each of the "
-                          f"{inp.B * inp.H} heads") + f" ({toks} {'entries' if is_op else 'tokens'}, {secs:.1f} s)"}
+        kind = w["kind"]
+        rate, toks, secs = {"chain": lambda: oracle_sample_chain(inp, args.cpu_seconds),
+                            "operator": lambda: oracle_sample_operator(inp, args.cpu_seconds),
+                            "position": lambda: oracle_sample_position(inp, args.cpu_seconds),
+                            "gate_prep": lambda: oracle_sample_gate(inp, args.cpu_seconds),
+                            "head": lambda: oracle_sample_head(inp, args.cpu_seconds)}[kind]()
+        sample = {"chain": f"{toks // inp.n} whole heads", "position": f"{toks // inp.n} whole heads",
+                  "gate_prep": f"{toks // inp.n} whole heads",
+                  "operator": f"{toks // (inp.n * inp.n)} whole heads' W",
+                  "head": f"{toks // (inp.B * inp.H)} seeded random rows of each of the {inp.B * inp.H} heads"}[kind]
+        cpu = {"value": rate, "unit": METRICS[kind][1], "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample + f" ({toks} {'entries' if kind == 'operator' else 'tokens'}, {secs:.1f} s)"}
 
     if rank == 0:
-        line = {"metric": ("chain tokens/s (B*H*n/s)" if is_chain else
-                           "operator entries/s (B*H*n*n/s)" if is_op else
-                           "position tokens/s (B*H*n/s)" if is_pos else "head tokens/s (B*H*n/s)"),
-                "value": value, "unit": "entries/s" if is_op else "tokens/s", "n_gpus": world, "steps": args.steps,
+        metric, unit = METRICS[w["kind"]]
+        line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32" if (is_chain or is_op) else "bf16" if is_pos else ("bf16" if inp.dtype == "bf16" else "f32->bf16"),
+                "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
                 "data": "synthetic (seeded, workloads.py)",
                 "config": dict(config_of(args, inp, world), l2="flushed between timed steps"),
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "roofline": roof, "classes": classes, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
                 "gpu_launches": launches_per_step * args.steps,
-                "kernel_ms_per_step": kern}
+                "kernel_ms_per_step": {str(k): v for k, v in sorted(per_kind.items())}}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -180,22 +180,31 @@ def last_launch_count() -> int:
     return int(lib().resolvent_last_launch_count())
 
 
-def gate_prep(u: torch.Tensor, theta: torch.Tensor, g: Switch, *, status=None, stream=None,
-              sync: bool = True) -> dict:
-    """Blended gates and block products of every head; u, theta fp32 [B,H,n]."""
+def gate_prep_outputs(B, H, n, device) -> dict:
+    """Output buffers of gate_prep: m, theta_p [B,H,n]; gate, prefix, suffix [B,H,n,2];
+    carry [B,H,ceil(n/128),2] (fp32, complex values as (re, im) pairs)."""
+    nb = (n + BLOCK - 1) // BLOCK
+    return {"m": torch.empty(B, H, n, device=device), "theta_p": torch.empty(B, H, n, device=device),
+            "gate": torch.empty(B, H, n, 2, device=device),
+            "prefix": torch.empty(B, H, n, 2, device=device),
+            "suffix": torch.empty(B, H, n, 2, device=device),
+            "carry": torch.empty(B, H, nb, 2, device=device)}
+
+
+def gate_prep(u: torch.Tensor, theta: torch.Tensor, g: Switch, *, out=None, status=None,
+              stream=None, sync: bool = True) -> dict:
+    """Blended gates and block products of every head; u, theta fp32 [B,H,n]. `out` (from
+    gate_prep_outputs) receives them; entries set to None are not written."""
     u = _dev(u, "u", torch.float32)
     theta = _dev(theta, "theta", torch.float32)
     B, H, n = u.shape
-    nb = (n + BLOCK - 1) // BLOCK
     sw, keep = _switches(H, 0.0, 0.0, g)
     dev = u.device
-    out = {"m": torch.empty(B, H, n, device=dev), "theta_p": torch.empty(B, H, n, device=dev),
-           "gate": torch.empty(B, H, n, 2, device=dev), "prefix": torch.empty(B, H, n, 2, device=dev),
-           "suffix": torch.empty(B, H, n, 2, device=dev),
-           "carry": torch.empty(B, H, nb, 2, device=dev)}
+    if out is None:
+        out = gate_prep_outputs(B, H, n, dev)
     st = status if status is not None else new_status(dev)
     _raise(lib().resolvent_gate_prep(_ptr(u), _ptr(theta), sw, B, H, n, *[
-        _ptr(out[k]) for k in ("m", "theta_p", "gate", "prefix", "suffix", "carry")],
+        _ptr(out.get(k)) for k in ("m", "theta_p", "gate", "prefix", "suffix", "carry")],
         _ptr(st), _stream(stream)))
     if sync and status is None:
         status_sync(st, stream)

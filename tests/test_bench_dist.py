@@ -92,15 +92,16 @@ def test_work_accounting_stops_at_fp32_underflow():
 
 def test_reference_arm_prints_one_contract_line():
     """`bench.py --impl reference` (the oracle timed on the host cores) prints exactly one JSON
-    line with the keys the driver reads, for the head and the position-only workloads."""
+    line with the keys the driver reads, for the head, position-only, gate-preparation and
+    mixed-switch workloads (small sizes)."""
     import json
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    for wl in ("tiny", "position"):
+    for wl in ("tiny", "position", "gate_prep", "mixed"):
         args = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
                 "--workload", wl, "--steps", "1", "--warmup", "0", "--cpu-seconds", "0.2"]
-        if wl == "position":
+        if wl in ("position", "gate_prep", "mixed"):
             args += ["--B", "1", "--H", "2", "--n", "512"]
         out = subprocess.run(args, capture_output=True, text=True, timeout=300, cwd=root)
         assert out.returncode == 0, out.stderr[-2000:]
@@ -115,3 +116,17 @@ def test_reference_arm_prints_one_contract_line():
         assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
         assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
         assert d["config"]["workload"] == wl
+
+
+def test_mixed_workload_dispatch_classes():
+    """The mixed grid (head h takes point h mod 27 of beta x qk x g): of 64 heads, 22 have
+    qk = 0 (O(n) readout), 14 have g = 0 and qk != 0 (the real fused kernel), 28 are gated."""
+    import bench
+    import workloads as W
+    hi = W.mixed(B=1, H=64, n=256)
+    c = bench.head_classes(hi)
+    assert (c["chain_heads"], c["real_heads"], c["gated_heads"]) == (22, 14, 28)
+    assert c["chain_tokens"] == 22 * 256
+    causal = 256 * 257 / 2
+    assert c["real_flops"] == 14 * causal * (2 * 128 + 2 * 128)
+    assert 0 < c["gated_live"] <= c["gated_causal"] == 28 * causal

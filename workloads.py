@@ -286,6 +286,34 @@ def position(B=4, H=32, n=8192) -> PositionInputs:
     return position_inputs(B, H, n, 128, seed=SEED_BASE + 6, name=f"position B{B} H{H} n{n} dv128")
 
 
+@dataclass
+class GateInputs:
+    """Gate-preparation inputs: u, theta [BH,n] fp32 and per-head g [H]."""
+    B: int
+    H: int
+    n: int
+    u: np.ndarray
+    theta: np.ndarray
+    g: np.ndarray
+    name: str = ""
+
+    def switches_bh(self):
+        return (np.zeros(self.B * self.H), np.zeros(self.B * self.H), np.tile(self.g, self.B))
+
+
+def gate_prep(B=1, H=64, n=32768) -> GateInputs:
+    """Gate preparation alone at the mixed-switch shape: the mixed workload's u ~ U(-0.5,1.5),
+    theta ~ U(-pi,pi) (same seed and streams) and its per-head g from the grid."""
+    seed = SEED_BASE + 4
+    BH = B * H
+    u = (-0.5 + 2.0 * uniform(seed, STREAM["u"], BH * n)).astype(np.float32).reshape(BH, n)
+    theta = (-math.pi + 2 * math.pi * uniform(seed, STREAM["theta"], BH * n)).astype(
+        np.float32).reshape(BH, n)
+    grid_g = [0.0, 0.3, 1.0]
+    g = np.array([grid_g[h % 3] for h in range(H)], dtype=np.float64)
+    return GateInputs(B, H, n, u, theta, g, f"gate prep B{B} H{H} n{n}")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "gated_softmax": gated_softmax,
@@ -294,4 +322,5 @@ WORKLOADS = {
     "mixed": mixed,
     "operator": operator_heads,
     "position": position,
+    "gate_prep": gate_prep,
 }
