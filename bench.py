@@ -629,7 +629,7 @@ def class_figures(w, inp, per_kind_ms, pk):
 def run_e2e(args, w, device, world, R):
     """The same metric end to end: every step uploads its inputs from pinned host memory, runs
     the call and reads its outputs back to pinned host memory, through the overlapped host
-    pipeline (uploads, calls, downloads on three streams, double-buffered device memory)."""
+    pipeline (uploads, calls and downloads on three streams, double-buffered device memory)."""
     import torch
     from gated_causal_attention_gb300.pipeline import HostPipeline
     pinned = [torch.from_numpy(np.ascontiguousarray(x).reshape(s)).to(dt).pin_memory()
@@ -646,10 +646,14 @@ def run_e2e(args, w, device, world, R):
     dist_barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(pipe.up)
+    e0.record(pipe.up[0])
+    for s in pipe.up[1:] + pipe.down + [pipe.comp]:
+        s.wait_event(e0)  # every stream of the timed steps starts after e0
     for i in range(args.steps):
         pipe.submit(pinned, host_out[i % 2])
-    e1.record(pipe.down)
+    for s in pipe.down[1:] + pipe.up + [pipe.comp]:
+        pipe.down[0].wait_stream(s)
+    e1.record(pipe.down[0])
     pipe.synchronize()
     e_ms = dist_max(e0.elapsed_time(e1) / args.steps, world, device)
     R.status_sync(w["status"])
