@@ -138,16 +138,31 @@ gate_prep_kernel(GatePrepArgs a, const __grid_constant__ HeadTable tab)
         a.carry[bh * nb + blk] = make_float2(block_total.re, block_total.im);
 }
 
+// Finiteness scans: 16-byte loads where a head's values start on a 16-byte boundary and fill
+// whole 16-byte units (the scan then runs at memory speed), one value at a time otherwise.
 __global__ void check_finite_bf16_kernel(const __nv_bfloat16 *x, int64_t per_head,
                                          const __grid_constant__ HeadTable tab, int32_t *status)
 {
     const int slot = blockIdx.y;
     if (slot >= tab.count) return;
     const uint16_t *p = reinterpret_cast<const uint16_t *>(x) + (int64_t)tab.bh[slot] * per_head;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
     bool bad = false;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_head;
-         i += (int64_t)gridDim.x * blockDim.x)
-        bad |= (p[i] & 0x7F80u) == 0x7F80u;  // exponent all ones: inf or NaN
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (per_head & 7) == 0) {
+        // eight values a load; a bf16 is inf or NaN when its exponent field (0x7F80) is all ones
+        const uint4 *p4 = reinterpret_cast<const uint4 *>(p);
+        uint32_t hit = 0u;
+#pragma unroll 4
+        for (int64_t i = t0; i < per_head / 8; i += stride) {
+            const uint4 w = __ldg(p4 + i);
+            hit |= __vcmpeq2(w.x & 0x7F807F80u, 0x7F807F80u) | __vcmpeq2(w.y & 0x7F807F80u, 0x7F807F80u) |
+                   __vcmpeq2(w.z & 0x7F807F80u, 0x7F807F80u) | __vcmpeq2(w.w & 0x7F807F80u, 0x7F807F80u);
+        }
+        bad = hit != 0u;
+    } else {
+        for (int64_t i = t0; i < per_head; i += stride)
+            bad |= (p[i] & 0x7F80u) == 0x7F80u;  // exponent all ones: inf or NaN
+    }
     if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, RS_STATUS_NONFINITE_BIT);
 }
 
@@ -157,10 +172,21 @@ __global__ void check_finite_f32_kernel(const float *x, int64_t per_head,
     const int slot = blockIdx.y;
     if (slot >= tab.count) return;
     const float *p = x + (int64_t)tab.bh[slot] * per_head;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
     bool bad = false;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_head;
-         i += (int64_t)gridDim.x * blockDim.x)
-        bad |= !isfinite(p[i]);
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (per_head & 3) == 0) {
+        const uint4 *p4 = reinterpret_cast<const uint4 *>(p);
+        uint32_t hit = 0u;
+#pragma unroll 4
+        for (int64_t i = t0; i < per_head / 4; i += stride) {
+            const uint4 w = __ldg(p4 + i);
+            hit |= ((w.x & 0x7F800000u) == 0x7F800000u) | ((w.y & 0x7F800000u) == 0x7F800000u) |
+                   ((w.z & 0x7F800000u) == 0x7F800000u) | ((w.w & 0x7F800000u) == 0x7F800000u);
+        }
+        bad = hit != 0u;
+    } else {
+        for (int64_t i = t0; i < per_head; i += stride) bad |= !isfinite(p[i]);
+    }
     if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, RS_STATUS_NONFINITE_BIT);
 }
 
@@ -238,7 +264,7 @@ cudaError_t launch_check_finite_bf16(const __nv_bfloat16 *x, int64_t per_head, c
                                      int32_t *status, cudaStream_t s)
 {
     if (tab.count == 0 || per_head == 0) return cudaSuccess;
-    const int gx = (int)std::min<int64_t>((per_head + 255) / 256, 64);
+    const int gx = (int)std::min<int64_t>((per_head + 256 * 32 - 1) / (256 * 32), 64);
     check_finite_bf16_kernel<<<dim3(gx, tab.count), 256, 0, s>>>(x, per_head, tab, status);
     return cudaGetLastError();
 }
@@ -247,7 +273,7 @@ cudaError_t launch_check_finite_f32(const float *x, int64_t per_head, const Head
                                     int32_t *status, cudaStream_t s)
 {
     if (tab.count == 0 || per_head == 0) return cudaSuccess;
-    const int gx = (int)std::min<int64_t>((per_head + 255) / 256, 64);
+    const int gx = (int)std::min<int64_t>((per_head + 256 * 16 - 1) / (256 * 16), 64);
     check_finite_f32_kernel<<<dim3(gx, tab.count), 256, 0, s>>>(x, per_head, tab, status);
     return cudaGetLastError();
 }

@@ -332,3 +332,26 @@ def test_operator_bounded_wait_reports_timeout(R, oracle_mod, launch, block):
         got = Wre[h][rows] + 1j * Wim[h][rows]
         ref = oracle_mod.operator_rows(hi.q[h], hi.k[h], hi.u[h], hi.theta[h], 1.0, 1.0, 0.5, rows)
         assert np.max(np.abs(got - ref)) <= W_TOL * np.max(np.abs(ref)), f"head {h}"
+
+
+# ------------------------------------------------------------------ refusal scan of qk = 0 heads
+
+
+@pytest.mark.parametrize("dtype,n,d", [("bf16", 64, 64), ("fp32", 64, 64), ("bf16", 301, 8), ("fp32", 301, 8)])
+def test_qk0_scan_finds_every_position(R, dtype, n, d):
+    """Heads with qk = 0 never form a logit, so their q and k are scanned for values that are
+    not finite ("Evaluation and refusals", the NonFinite refusal). The scan reads 16-byte units
+    (eight bf16 or four fp32 values): a NaN or an infinity at each of the eight positions of a
+    unit, in q or in k, in the second head, must refuse; the same inputs with finite values must
+    not."""
+    base = W.head_inputs(1, 2, n, d, d, seed=31, beta=0.5, qk=0.0, g=0.3)
+    base.dtype = dtype
+    run_head(R, base)  # every value finite: no refusal
+    bad_values = [np.nan, np.inf, -np.inf]
+    for pos in range(8):
+        hi = W.head_inputs(1, 2, n, d, d, seed=31, beta=0.5, qk=0.0, g=0.3)
+        hi.dtype = dtype
+        x = hi.q if pos % 2 == 0 else hi.k
+        x.reshape(-1)[n * d + 8 * (pos + 3) + pos] = bad_values[pos % 3]  # head 1, lane pos of a unit
+        with pytest.raises(R.NonFinite):
+            run_head(R, hi)
