@@ -265,8 +265,9 @@ rs_status resolvent_gate_prep(const float *u, const float *theta, rs_switches sw
                           (const void *)block_carry})
         if (p && !aligned16(p)) return RS_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    prof_mark(s, 0, RS_PROF_GATE_PREP);
-    for (const HeadTable &t : tables_for(sw, B, H, [](const Sw &) { return true; })) {
+    const auto tabs = tables_for(sw, B, H, [](const Sw &) { return true; });
+    prof_mark(s, 0, RS_PROF_GATE_PREP);  // after the host-side tables: the pair brackets the launches
+    for (const HeadTable &t : tabs) {
         GatePrepArgs a{};
         a.u = u; a.theta = theta; a.n = n; a.m = m; a.theta_p = theta_p;
         a.gate = reinterpret_cast<float2 *>(gate);
