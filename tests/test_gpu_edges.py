@@ -151,6 +151,25 @@ def test_running_maximum_growing_in_small_steps(R, oracle_mod, g):
     close_per_head(re + 1j * im, oracle_head(oracle_mod, hi), O_TOL, f"g={g}")
 
 
+@pytest.mark.parametrize("d,col,j,sign", [(64, 60, 5, 1.0), (64, 17, 40, -1.0),
+                                           (128, 100, 77, 1.0), (128, 3, 126, -1.0)])
+def test_running_maximum_jumps_on_a_later_tile(R, oracle_mod, d, col, j, sign):
+    """Gated head (g = 0.5, beta = 1, qk = +-1), n = 384: the query rows of the last block see
+    small logits on key tile 1 (their first tile) and, on key tile 0, one key whose single
+    element at column `col` makes a logit of 2400 / sqrt(d) nats (300 or 212). The running
+    maximum must move on that later tile, or P = 2^{t - M} overflows. The big element sits in
+    either 64-column half of K and Q, at key rows of different warps, with qk of either sign.
+    Every row against the oracle."""
+    n = 384
+    hi = W.head_inputs(1, 1, n, d, d, seed=39, q_scale=1 / math.sqrt(d), u_range=(0.97, 1.0),
+                       theta_range=(-0.1, 0.1), beta=1.0, qk=sign, g=0.5)
+    hi.q[:, 256:, col] = 4.0
+    hi.k[:, j, col] = 600.0 * sign
+    re, im = run_head(R, hi)
+    assert np.all(np.isfinite(re)) and np.all(np.isfinite(im))
+    close_per_head(re + 1j * im, oracle_head(oracle_mod, hi), O_TOL, f"d={d} col={col} j={j}")
+
+
 # ------------------------------------------------------------------ overflow away from beta = 1
 
 
