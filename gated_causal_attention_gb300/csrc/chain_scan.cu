@@ -9,11 +9,15 @@
 //   1. the chunk of b arrives in shared memory by one bulk copy; the gates are formed;
 //   2. each of 8 warps runs the recurrence over its 16 tokens from a zero carry and keeps
 //      the affine map (A_w, Y_w) of its stretch: y_out = A_w y_in + Y_w;
-//   3. warp 0 composes the 8 maps into the chunk's map and publishes it; then looks back
-//      over earlier chunks of the same head (their maps, or the carry a chunk already
-//      resolved) until it knows y at the end of the previous chunk, and publishes its own
-//      resolved carry. A map with A = 0 (a closed gate) ends the look-back early;
-//   4. every warp reruns its stretch from the true carry and writes y.
+//   3. warp 0 composes the 8 maps into the chunk's map and hands it to warp 1, which
+//      publishes it; meanwhile warp 0 looks back over earlier chunks of the same head (their
+//      maps, or the carry a chunk already resolved) until it knows y at the end of the
+//      previous chunk. A map with A = 0 (a closed gate) ends the look-back early;
+//   4. every warp reruns its stretch from the true carry and writes y; warp 0 first
+//      publishes the chunk's resolved carry.
+// Publication is a release store of the chunk's flag after the data (a __syncwarp orders
+// the other lanes' stores before it), and reading is an acquire load of the flag followed
+// by a __syncwarp before the data loads; no other fence.
 // b is read once and y written once. Every wait on another chunk is bounded in time and
 // sets RS_STATUS_TIMEOUT (carry taken as 0) when it runs out, so the kernel always ends.
 #include <mutex>
@@ -26,6 +30,14 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kTokPerWarp = kChainChunk / kWarps;  // 16
+constexpr int kBarMap = 1;  // named barrier: warp 0 hands the chunk's map to warp 1
+
+// Arrival without waiting (the producer side of a hand-off through shared memory: the
+// barrier's completion orders this thread's earlier accesses before the waiting threads').
+__device__ __forceinline__ void named_bar_arrive(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 template <typename BT>
 __device__ __forceinline__ float load_val(const BT *p);
@@ -50,6 +62,8 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     __shared__ float s_m[kChainChunk];
     __shared__ float s_wAz[kWarps], s_wYz[kWarps], s_exAz[kWarps], s_exYz[kWarps];
     __shared__ float s_zin;
+    __shared__ cplx s_mapA;
+    __shared__ float2 s_mapZ;
 
     const int dv = a.dv, n = a.n;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -59,6 +73,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     cplx *s_warpY = reinterpret_cast<cplx *>(smem + sizeof(BT) * kChainChunk * dv);  // [8][dv]
     cplx *s_exY = s_warpY;  // the exclusive prefixes replace the warps' maps in place
     cplx *s_yin = s_warpY + kWarps * dv;                                        // [dv]
+    cplx *s_map = s_yin + dv;  // [dv] the chunk's map, handed from warp 0 to warp 1
 
     if (tid == 0) {
         s_ticket = atomicAdd(a.counter, 1);
@@ -164,12 +179,17 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     }
     __syncthreads();
 
+    // warp 0: the chunk's map (eA, eY; eAz, eYz for the normaliser) and the carry into the
+    // chunk (yin, zin)
+    cplx eA = {1.f, 0.f};
+    cplx eY[CPL], yin[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) eY[c] = yin[c] = {0.f, 0.f};
+    float eAz = 1.f, eYz = 0.f, zin = 0.f;
+    const int64_t me = (int64_t)slot * nchunks + chunk;
+    const bool publish = ticket != a.withhold_chunk;
     if (warp == 0) {
         // compose the warps' maps: exclusive prefixes and the chunk's map
-        cplx eA = {1.f, 0.f};
-        cplx eY[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) eY[c] = {0.f, 0.f};
         for (int w = 0; w < kWarps; ++w) {
             if (lane == 0) s_exA[w] = eA;
             const cplx wA = s_warpA[w];
@@ -184,7 +204,6 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
             }
             eA = cmul(wA, eA);
         }
-        float eAz = 1.f, eYz = 0.f;
         if (NORM) {
             for (int w = 0; w < kWarps; ++w) {
                 if (lane == 0) {
@@ -195,14 +214,17 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                 eAz *= s_wAz[w];
             }
         }
-        float zin = 0.f;
-
-        const int64_t me = (int64_t)slot * nchunks + chunk;
-        const bool publish = ticket != a.withhold_chunk;
-        cplx yin[CPL];
+        if (chunk > 0 && publish) {
+            // warp 1 publishes the chunk's map while this warp looks back
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) yin[c] = {0.f, 0.f};
-
+            for (int c = 0; c < CPL; ++c)
+                if (ch0 + c < dv) s_map[ch0 + c] = eY[c];
+            if (lane == 0) {
+                s_mapA = eA;
+                s_mapZ = make_float2(eAz, eYz);
+            }
+            named_bar_arrive(kBarMap, 64);
+        }
         if (chunk == 0) {
             // before the first chunk: the carry of the previous segment, or nothing
             if (a.carry_in) {
@@ -213,29 +235,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                         yin[c] = {v.x, v.y};
                     }
             }
-            if (publish) {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const cplx t = cmul(eA, yin[c]);
-                    if (ch0 + c < dv)
-                        a.incl_y[me * dv + ch0 + c] = make_float2(t.re + eY[c].re, t.im + eY[c].im);
-                }
-                if (NORM && lane == 0) a.incl_z[me] = eYz;
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(a.flags + me, 2);
-            }
         } else {
-            if (publish) {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c)
-                    if (ch0 + c < dv) a.agg_y[me * dv + ch0 + c] = make_float2(eY[c].re, eY[c].im);
-                if (lane == 0) a.agg_a[me] = make_float2(eA.re, eA.im);
-                if (NORM && lane == 0) a.agg_z[me] = make_float2(eAz, eYz);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(a.flags + me, 1);
-            }
             // look back: acc maps y_end(p) to y_end(chunk-1) (and z likewise)
             float accAz = 1.f, accYz = 0.f;
             cplx accA = {1.f, 0.f};
@@ -244,20 +244,20 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
             for (int c = 0; c < CPL; ++c) accY[c] = {0.f, 0.f};
             for (int p = chunk - 1; p >= 0; --p) {
                 const int64_t other = (int64_t)slot * nchunks + p;
-                int f = 0;
-                if (lane == 0) {
-                    f = ld_acquire_gpu(a.flags + other);
-                    if (f == 0) {
+                int f = lane == 0 ? ld_acquire_gpu(a.flags + other) : 0;
+                f = __shfl_sync(0xffffffffu, f, 0);
+                if (f == 0) {
+                    if (lane == 0) {
                         const uint64_t t0 = globaltimer_ns();
                         while ((f = ld_acquire_gpu(a.flags + other)) == 0) {
                             if (globaltimer_ns() - t0 > a.wait_limit_ns) break;
                             __nanosleep(64);
                         }
                     }
+                    f = __shfl_sync(0xffffffffu, f, 0);
                 }
-                f = __shfl_sync(0xffffffffu, f, 0);
+                // lane 0's acquire, then __syncwarp: the other lanes' loads below come after it
                 __syncwarp();
-                __threadfence();
                 if (f == 0) {  // ran out of time: take the carry as 0 and say so
                     if (lane == 0) flag_status(a.status, RS_STATUS_TIMEOUT_BIT);
 #pragma unroll
@@ -303,26 +303,43 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                     break;
                 }
             }
-            if (publish) {
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const cplx t = cmul(eA, yin[c]);
-                    if (ch0 + c < dv)
-                        a.incl_y[me * dv + ch0 + c] =
-                            make_float2(t.re + eY[c].re, t.im + eY[c].im);
-                }
-                if (NORM && lane == 0) a.incl_z[me] = fmaf(eAz, zin, eYz);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(a.flags + me, 2);
-            }
         }
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
             if (ch0 + c < dv) s_yin[ch0 + c] = yin[c];
         if (lane == 0) s_zin = zin;
+    } else if (warp == 1 && chunk > 0 && publish) {
+        // the chunk's map (flag 1), so that later chunks can look past this one before its
+        // carry is resolved; __syncwarp orders every lane's stores before lane 0's release
+        named_bar_sync(kBarMap, 64);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (ch0 + c < dv) {
+                const cplx m = s_map[ch0 + c];
+                a.agg_y[me * dv + ch0 + c] = make_float2(m.re, m.im);
+            }
+        if (lane == 0) {
+            a.agg_a[me] = make_float2(s_mapA.re, s_mapA.im);
+            if (NORM) a.agg_z[me] = s_mapZ;
+        }
+        __syncwarp();
+        if (lane == 0) st_release_gpu(a.flags + me, 1);
     }
     __syncthreads();
+    // the resolved carry y_end(chunk) = eA y_in + eY, published after the barrier: the
+    // release waits for warp 0's stores to complete, and the other warps write y meanwhile
+    if (warp == 0 && publish) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const cplx t = cmul(eA, yin[c]);
+            if (ch0 + c < dv)
+                a.incl_y[me * dv + ch0 + c] = make_float2(t.re + eY[c].re, t.im + eY[c].im);
+        }
+        if (NORM && lane == 0) a.incl_z[me] = fmaf(eAz, zin, eYz);
+        // __syncwarp orders every lane's stores before lane 0's release of the flag
+        __syncwarp();
+        if (lane == 0) st_release_gpu(a.flags + me, 2);
+    }
 
     // pass 2: rerun each stretch from its true carry and write y
     {
@@ -389,7 +406,7 @@ template <int CPL, typename BT, bool NORM>
 cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 {
     const int nchunks = (a.n + kChainChunk - 1) / kChainChunk;
-    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (kWarps + 1) * a.dv;
+    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (kWarps + 2) * a.dv;
     auto k = chain_scan_kernel<CPL, BT, NORM>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
