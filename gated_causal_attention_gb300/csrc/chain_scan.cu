@@ -49,17 +49,17 @@ __device__ __forceinline__ float load_val<__nv_bfloat16>(const __nv_bfloat16 *p)
     return __bfloat162float(*p);
 }
 
+// CTAs per SM that registers and shared memory both allow: six at dv <= 64, four at
+// dv = 128 with bf16 b, three with fp32 b
 template <int CPL, typename BT, bool NORM>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, CPL <= 2 ? 6 : (sizeof(BT) == 2 ? 4 : 3))
 chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_ticket;
     __shared__ __align__(8) uint64_t s_bar;
-    __shared__ cplx s_gate[kChainChunk];
     __shared__ cplx s_warpA[kWarps], s_exA[kWarps];
-    // the normaliser chain z_i = m_i z_{i-1} + 1 (qk = 0 readout): gate moduli, warp maps
-    __shared__ float s_m[kChainChunk];
+    // the normaliser chain z_i = m_i z_{i-1} + 1 (qk = 0 readout): warp maps
     __shared__ float s_wAz[kWarps], s_wYz[kWarps], s_exAz[kWarps], s_exYz[kWarps];
     __shared__ float s_zin;
     __shared__ cplx s_mapA;
@@ -73,7 +73,9 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     cplx *s_warpY = reinterpret_cast<cplx *>(smem + sizeof(BT) * kChainChunk * dv);  // [8][dv]
     cplx *s_exY = s_warpY;  // the exclusive prefixes replace the warps' maps in place
     cplx *s_yin = s_warpY + kWarps * dv;                                        // [dv]
-    cplx *s_map = s_yin + dv;  // [dv] the chunk's map, handed from warp 0 to warp 1
+    // warp 0's exclusive prefix is the identity (never stored); its slot carries the chunk's
+    // map from warp 0 to warp 1
+    cplx *s_map = s_warpY;
 
     if (tid == 0) {
         s_ticket = atomicAdd(a.counter, 1);
@@ -103,13 +105,17 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int e = tid; e < len * dv; e += blockDim.x) sb[e] = bsrc[e];
     }
 
-    // gates of this chunk ("Object": blended gate and gate)
+    // gates of this chunk ("Object": blended gate and gate): lane l < 16 of warp w holds the
+    // gate of token 16 w + l (and its modulus) for the warp's two passes
+    const int tok0 = warp * kTokPerWarp;
     bool bad = false;
-    if (tid < kChainChunk) {
-        const int t = s0 + tid;
+    cplx gate = {1.f, 0.f};
+    float gmod = 1.f;
+    if (lane < kTokPerWarp) {
+        const int t = s0 + tok0 + lane;
         cplx at = {1.f, 0.f};
         float mt = 1.f;
-        if (tid < len) {
+        if (tok0 + lane < len) {
             const float uu = a.u[bh * n + t], th = a.theta[bh * n + t];
             const float m = fminf(fmaxf(fmaf(g, uu, 1.f - g), 0.f), 1.f);
             const float tp = g * th;
@@ -123,8 +129,8 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
                 mt = 0.f;
             }
         }
-        s_gate[tid] = at;
-        s_m[tid] = mt;
+        gate = at;
+        gmod = mt;
     }
     if (__syncthreads_or(bad) && tid == 0) flag_status(a.status, RS_STATUS_NONFINITE_BIT);
     __shared__ int s_loaded;
@@ -141,7 +147,6 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     if (!s_loaded) return;  // the chunk never arrived: give up on it (uniform across the CTA)
 
     const int ch0 = lane * CPL;
-    const int tok0 = warp * kTokPerWarp;
     const int tok1 = min(tok0 + kTokPerWarp, len);
 
     // pass 1: each warp's stretch as an affine map from a zero carry
@@ -151,7 +156,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
 #pragma unroll
         for (int c = 0; c < CPL; ++c) y[c] = {0.f, 0.f};
         for (int t = tok0; t < tok1; ++t) {
-            const cplx at = s_gate[t];
+            const cplx at = shfl_idx(gate, t - tok0);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const float bv = (ch0 + c < dv) ? load_val(sb + t * dv + ch0 + c) : 0.f;
@@ -167,7 +172,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         if (NORM) {  // the same stretch of the real chain (every lane alike)
             float Az = 1.f, Yz = 0.f;
             for (int t = tok0; t < tok1; ++t) {
-                const float m = s_m[t];
+                const float m = __shfl_sync(0xffffffffu, gmod, t - tok0);
                 Yz = fmaf(m, Yz, 1.f);
                 Az *= m;
             }
@@ -349,7 +354,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int c = 0; c < CPL; ++c) {
             if (ch0 + c < dv) {
                 const cplx t = cmul(wA, s_yin[ch0 + c]);
-                const cplx e = s_exY[warp * dv + ch0 + c];
+                const cplx e = warp == 0 ? cplx{0.f, 0.f} : s_exY[warp * dv + ch0 + c];
                 y[c] = {t.re + e.re, t.im + e.im};
             } else {
                 y[c] = {0.f, 0.f};
@@ -362,12 +367,12 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         const bool scale_out = NORM && beta != 0.f;
         float z = NORM ? fmaf(s_exAz[warp], s_zin, s_exYz[warp]) : 0.f;
         for (int t = tok0; t < tok1; ++t) {
-            const cplx at = s_gate[t];
+            const cplx at = shfl_idx(gate, t - tok0);
             float vr[CPL], vi[CPL];
             const bool last = a.carry_out && s0 + t == n - 1;
             float fz = 1.f;
             if (scale_out) {
-                z = fmaf(s_m[t], z, 1.f);
+                z = fmaf(__shfl_sync(0xffffffffu, gmod, t - tok0), z, 1.f);
                 fz = exp2f(-beta * log2f(z));
             }
 #pragma unroll
@@ -406,9 +411,13 @@ template <int CPL, typename BT, bool NORM>
 cudaError_t launch_t(const ChainArgs &a, const HeadTable &tab, cudaStream_t s)
 {
     const int nchunks = (a.n + kChainChunk - 1) / kChainChunk;
-    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (kWarps + 2) * a.dv;
+    const size_t smem = sizeof(BT) * kChainChunk * a.dv + sizeof(cplx) * (kWarps + 1) * a.dv;
     auto k = chain_scan_kernel<CPL, BT, NORM>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // all of the SM's unified L1 / shared memory as shared memory: six CTAs of 128 tokens x 64
+    // fp32 channels fit
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     k<<<tab.count * nchunks, 256, smem, s>>>(a, tab);
     return cudaGetLastError();
