@@ -7,8 +7,9 @@
 // Each CTA takes a ticket (an atomic counter, so tickets follow the order CTAs start in)
 // and owns one chunk of 128 tokens x dv channels of one head:
 //   1. the chunk of b arrives in shared memory by one bulk copy; the gates are formed;
-//   2. each of 8 warps runs the recurrence over its 16 tokens from a zero carry and keeps
-//      the affine map (A_w, Y_w) of its stretch: y_out = A_w y_in + Y_w;
+//   2. each of 8 warps runs the recurrence over its stretch of tokens (2 for warp 0, 18 for
+//      the others) from a zero carry and keeps the affine map (A_w, Y_w) of its stretch:
+//      y_out = A_w y_in + Y_w;
 //   3. warp 0 composes the 8 maps into the chunk's map and hands it to warp 1, which
 //      publishes it; meanwhile warp 0 looks back over earlier chunks of the same head (their
 //      maps, or the carry a chunk already resolved) until it knows y at the end of the
@@ -29,7 +30,12 @@ namespace rs {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kTokPerWarp = kChainChunk / kWarps;  // 16
+// Stretches: warp 0 takes 2 tokens and warps 1-7 take 18 each, because warp 0 also looks
+// back and publishes the chunk's carry (whose release waits for its stores to complete)
+// while the others run their stretches.
+constexpr int kTok0 = 2, kTokW = 18;
+static_assert(kTok0 + (kWarps - 1) * kTokW == kChainChunk, "stretches cover the chunk");
+__device__ __forceinline__ int stretch_begin(int w) { return w == 0 ? 0 : kTok0 + (w - 1) * kTokW; }
 constexpr int kBarMap = 1;  // named barrier: warp 0 hands the chunk's map to warp 1
 
 // Arrival without waiting (the producer side of a hand-off through shared memory: the
@@ -105,13 +111,14 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         for (int e = tid; e < len * dv; e += blockDim.x) sb[e] = bsrc[e];
     }
 
-    // gates of this chunk ("Object": blended gate and gate): lane l < 16 of warp w holds the
-    // gate of token 16 w + l (and its modulus) for the warp's two passes
-    const int tok0 = warp * kTokPerWarp;
+    // gates of this chunk ("Object": blended gate and gate): lane l of a warp holds the gate
+    // of token l of its stretch (and its modulus) for the warp's two passes
+    const int tok0 = stretch_begin(warp);
+    const int ntok = warp == 0 ? kTok0 : kTokW;
     bool bad = false;
     cplx gate = {1.f, 0.f};
     float gmod = 1.f;
-    if (lane < kTokPerWarp) {
+    if (lane < ntok) {
         const int t = s0 + tok0 + lane;
         cplx at = {1.f, 0.f};
         float mt = 1.f;
@@ -147,7 +154,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
     if (!s_loaded) return;  // the chunk never arrived: give up on it (uniform across the CTA)
 
     const int ch0 = lane * CPL;
-    const int tok1 = min(tok0 + kTokPerWarp, len);
+    const int tok1 = min(tok0 + ntok, len);
 
     // pass 1: each warp's stretch as an affine map from a zero carry
     {
