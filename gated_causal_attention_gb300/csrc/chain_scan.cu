@@ -38,6 +38,8 @@ static_assert(kTok0 + (kWarps - 1) * kTokW == kChainChunk, "stretches cover the 
 __device__ __forceinline__ int stretch_begin(int w) { return w == 0 ? 0 : kTok0 + (w - 1) * kTokW; }
 constexpr int kBarMap = 1;  // named barrier: warp 0 hands the chunk's map to warp 1
 
+__device__ __forceinline__ cplx to_cplx(float2 v) { return {v.x, v.y}; }
+
 // Arrival without waiting (the producer side of a hand-off through shared memory: the
 // barrier's completion orders this thread's earlier accesses before the waiting threads').
 __device__ __forceinline__ void named_bar_arrive(int id, int count)
@@ -242,10 +244,7 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
             if (a.carry_in) {
 #pragma unroll
                 for (int c = 0; c < CPL; ++c)
-                    if (ch0 + c < dv) {
-                        const float2 v = a.carry_in[bh * dv + ch0 + c];
-                        yin[c] = {v.x, v.y};
-                    }
+                    if (ch0 + c < dv) yin[c] = to_cplx(a.carry_in[bh * dv + ch0 + c]);
             }
         } else {
             // look back: acc maps y_end(p) to y_end(chunk-1) (and z likewise)
