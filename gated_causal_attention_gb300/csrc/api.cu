@@ -373,6 +373,8 @@ rs_status resolvent_head_forward(const void *q, const void *k, const float *u, c
             ha.tma_out = tma_out ? 1 : 0;
             ha.numkv = reinterpret_cast<int *>(ws + w.numkv);
             ha.withhold = g_head_withhold;
+            // one block per SM: the block that starts about when this one ends is one SM count on
+            ha.prefetch_ahead = device_sm_count();
             // about 24 MB of K and V per head group: a group's K/V tiles stay in L2
             const size_t kv_head = (size_t)n * (DP + DVP) * 2;
             ha.heads_per_group = (int)std::max<size_t>(1, std::min<size_t>(t.count, (24u << 20) / kv_head));

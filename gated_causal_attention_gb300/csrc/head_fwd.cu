@@ -67,6 +67,14 @@ struct Roles {
 // softmax warps (one per half) that hold rows 32q..32q+31.
 constexpr int kBarSoftmax = 1, kBarVprep = 2, kBarRows0 = 3;
 
+// A tile of a tensor map into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 template <int DP, int DVP, bool GATED>
 struct Cfg {
     static constexpr uint32_t q_bytes = (DP / 64) * kRegion;
@@ -218,6 +226,26 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RL::prod_regs));
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
+        // The block that starts about when this one ends (one block per SM: block index plus
+        // the SM count) finds its Q tile and first K and V tiles in L2: prefetched once this
+        // block's own first tile is on its way.
+        auto prefetch_next = [&]() {
+            const int nb = (int)blockIdx.x + a.prefetch_ahead;
+            if (a.prefetch_ahead <= 0 || nb >= (int)gridDim.x) return;
+            const int ngrp = nb / (G * nqt);
+            const int nrem = nb - ngrp * G * nqt;
+            const int ngsz = min(G, tab.count - ngrp * G);
+            const int nQB = nqt - 1 - nrem / ngsz;
+            const int nslot = ngrp * G + nrem % ngsz;
+            const int nbh = tab.bh[nslot];
+            const int nkv = GATED ? a.numkv[nslot * nqt + nQB] : nQB;
+            const int nkb = nkv > 0 ? nQB - 1 : nQB;
+            for (int rr = 0; rr < DP / 64; ++rr) {
+                tma_prefetch_l2_3d(&maps.q, rr * 64, nQB * 128, nbh);
+                tma_prefetch_l2_3d(&maps.k, rr * 64, nkb * 128, nbh);
+            }
+            for (int rr = 0; rr < DVP / 64; ++rr) tma_prefetch_l2_3d(&maps.v, rr * 64, nkb * 128, nbh);
+        };
         if (lane == 0 && L::split) {  // the K ring
             int issued = 0;
             for (int t = 0; t < T; ++t) {
@@ -230,6 +258,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 for (int rr = 0; rr < DP / 64; ++rr)
                     tma_load_3d(stg + rr * kRegion, &maps.k, B.full + st, rr * 64, kb * 128, bh);
                 ++issued;
+                if (t == 0) prefetch_next();
             }
             drain_loads(B.full, L::NSK, issued);
         } else if (lane == 0) {
@@ -246,6 +275,7 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 for (int rr = 0; rr < DVP / 64; ++rr)
                     tma_load_3d(stg + L::k_bytes + rr * kRegion, &maps.v, B.full + st, rr * 64, kb * 128, bh);
                 ++issued;
+                if (t == 0) prefetch_next();
             }
             drain_loads(B.full, NS, issued);
         }

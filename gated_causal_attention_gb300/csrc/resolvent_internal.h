@@ -92,6 +92,7 @@ struct HeadArgs {
     int heads_per_group;  // blocks are ordered head group by head group (1 <= it <= table count)
     int *numkv;           // [slots * nqt] off-diagonal key tiles of each query tile (gated heads)
     int withhold;         // test knob: this block's K/V loads stop after its first tile (-1: none)
+    int prefetch_ahead;   // this block prefetches into L2 the first tiles of block + this (0: none)
 };
 // The tensor maps of one head launch: q, k, v (bf16, box 64 x 128).
 struct HeadMaps {
