@@ -371,16 +371,29 @@ chain_scan_kernel(ChainArgs a, const __grid_constant__ HeadTable tab)
         // qk = 0 readout: O_i = y_i z_i^{-beta}
         const float beta = tab.beta[slot];
         const bool scale_out = NORM && beta != 0.f;
-        float z = NORM ? fmaf(s_exAz[warp], s_zin, s_exYz[warp]) : 0.f;
+        // z_i = m_i z_{i-1} + 1 at each token of the stretch: lane l composes the maps
+        // x -> m x + 1 of tokens tok0 .. tok0 + l (a warp scan), applies them to z at the end of
+        // the previous stretch, and works out its token's factor z^{-beta} once
+        float fz_lane = 1.f;
+        if (scale_out) {
+            const bool mine = lane < tok1 - tok0;
+            float A = mine ? gmod : 1.f, Bz = mine ? 1.f : 0.f;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const float Ap = __shfl_up_sync(0xffffffffu, A, d), Bp = __shfl_up_sync(0xffffffffu, Bz, d);
+                if (lane >= d) {
+                    Bz = fmaf(A, Bp, Bz);
+                    A *= Ap;
+                }
+            }
+            const float zl = fmaf(A, fmaf(s_exAz[warp], s_zin, s_exYz[warp]), Bz);
+            fz_lane = exp2f(-beta * log2f(zl));
+        }
         for (int t = tok0; t < tok1; ++t) {
             const cplx at = shfl_idx(gate, t - tok0);
             float vr[CPL], vi[CPL];
             const bool last = a.carry_out && s0 + t == n - 1;
-            float fz = 1.f;
-            if (scale_out) {
-                z = fmaf(__shfl_sync(0xffffffffu, gmod, t - tok0), z, 1.f);
-                fz = exp2f(-beta * log2f(z));
-            }
+            const float fz = scale_out ? __shfl_sync(0xffffffffu, fz_lane, t - tok0) : 1.f;
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const float bv = (ch0 + c < dv) ? load_val(sb + t * dv + ch0 + c) : 0.f;
