@@ -67,6 +67,28 @@ struct Roles {
 // softmax warps (one per half) that hold rows 32q..32q+31.
 constexpr int kBarSoftmax = 1, kBarVprep = 2, kBarRows0 = 3;
 
+// (acc_re + i acc_im) <- z * (acc_re + i acc_im) over columns [c0, c1) of a row whose Re
+// block starts at trow and Im block at trow + dvp (32 columns at a time)
+__device__ __forceinline__ void cscale_acc_cols(uint32_t trow, int dvp, int c0, int c1, cplx z)
+{
+#pragma unroll 1
+    for (int cc = c0; cc < c1; cc += 32) {
+        uint32_t re[32], im[32];
+        RS_TMEM_LD32(trow + cc, re);
+        RS_TMEM_LD32(trow + dvp + cc, im);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const cplx x = cmul(z, {__uint_as_float(re[e]), __uint_as_float(im[e])});
+            re[e] = __float_as_uint(x.re);
+            im[e] = __float_as_uint(x.im);
+        }
+        RS_TMEM_ST32(trow + cc, re);
+        RS_TMEM_ST32(trow + dvp + cc, im);
+    }
+    tmem_st_wait();
+}
+
 // A tile of a tensor map into L2 only (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z)
 {
@@ -764,11 +786,12 @@ head_fwd_kernel(HeadArgs a, const __grid_constant__ HeadTable tab,
                 tmem_st_wait();
                 // the accumulator holds every off-diagonal P V: it takes alpha and (gated) the
                 // row factor prefix_i, once the last of them is done
-                if (h == 0 && numkv > 0 && (GATED || __any_sync(0xffffffffu, alpha != 1.f))) {
+                // (gated: each half takes half of the columns)
+                if ((GATED || h == 0) && numkv > 0 && (GATED || __any_sync(0xffffffffu, alpha != 1.f))) {
                     if (wait_bar_warp(B.pv_done + (t - 1) % L::NSB, ((t - 1) / L::NSB) & 1, s_abort, a.status)) {
                         tc_fence_after();
                         if (GATED)
-                            cscale_acc_row(trow, DVP, cmul(pq, {alpha, 0.f}));
+                            cscale_acc_cols(trow, DVP, h * (DVP / 2), (h + 1) * (DVP / 2), cmul(pq, {alpha, 0.f}));
                         else
                             scale_acc_row(trow, L::acc_cols, alpha);
                     } else {
