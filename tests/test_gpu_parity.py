@@ -235,6 +235,34 @@ def test_head_matches_oracle(R, oracle_mod, case):
         assert np.all(O.imag == 0)  # g = 0 removes the gates exactly: no imaginary part
 
 
+def test_heads_spanning_several_tables(R, oracle_mod):
+    """B=3 H=100 n=200 d=dv=64: 150 gated heads (h < 50) and 150 g = 0 heads, more than one
+    launch table (128 heads) per class; every row of every head against the oracle."""
+    H = 100
+    g = [0.5 if h < 50 else 0.0 for h in range(H)]
+    hi = W.head_inputs(3, H, 200, 64, 64, seed=61, q_scale=1 / 8, u_range=(0.9, 1.0),
+                       beta=1.0, qk=1.0, g=g)
+    O = run_head(R, hi)
+    rows = np.arange(hi.n)
+    assert_head_close(O, oracle_rows(oracle_mod, hi, rows), rows, "several tables")
+
+
+def test_chain_spanning_several_tables(R, oracle_mod):
+    """B=2 H=100 (200 heads, two launch tables) n=300 dv=16, every output."""
+    B, H, n, dv = 2, 100, 300, 16
+    r = np.random.default_rng(62)
+    b = r.standard_normal((B * H, n, dv)).astype(np.float32)
+    u = r.uniform(0.9, 1.0, (B * H, n)).astype(np.float32)
+    th = r.uniform(-math.pi, math.pi, (B * H, n)).astype(np.float32)
+    gs = [1.0 if h % 2 else 0.5 for h in range(H)]
+    yr, yi = R.chain_scan(dev(u.reshape(B, H, n)), dev(th.reshape(B, H, n)), gs,
+                          dev(b.reshape(B, H, n, dv)))
+    y = (yr.cpu().double().numpy() + 1j * yi.cpu().double().numpy()).reshape(B * H, n, dv)
+    ref, env, st = oracle_mod.chain_heads(u, th, f32(gs * B), b)
+    assert np.all(st == 0)
+    check_chain(y, ref, env)
+
+
 def test_mixed_switch_grid_small(R, oracle_mod):
     """Every point of the beta x qk x g grid (27 heads), every row, n = 300 and d = 128."""
     hi = W.mixed(B=1, H=27, n=300)
