@@ -491,6 +491,23 @@ def test_operator_matches_oracle(R, oracle_mod, case):
         assert np.all(np.triu(Wg[h], 1) == 0)
 
 
+def test_operator_spanning_several_tables(R, oracle_mod):
+    """B=2 H=80 (160 heads, two launch tables) n=130 d=64 bf16, every entry of W."""
+    B, H, n, d = 2, 80, 130, 64
+    hi = W.head_inputs(B, H, n, d, 8, seed=63, q_scale=1 / 8, u_range=(0.5, 1.0), zero_frac=0.02,
+                       beta=1.0, qk=1.0, g=0.5)
+    shp = (B, H, n)
+    Wre, Wim = R.operator(dev(hi.q.reshape(*shp, d), torch.bfloat16),
+                          dev(hi.k.reshape(*shp, d), torch.bfloat16),
+                          dev(hi.u.reshape(shp)), dev(hi.theta.reshape(shp)), 1.0, 1.0, 0.5)
+    torch.cuda.synchronize()
+    Wg = (Wre.cpu().double().numpy() + 1j * Wim.cpu().double().numpy()).reshape(B * H, n, n)
+    for h in range(B * H):
+        ref = oracle_mod.operator(hi.q[h], hi.k[h], hi.u[h], hi.theta[h], 1.0, 1.0, 0.5)
+        assert np.max(np.abs(Wg[h] - ref)) <= 1e-3 * np.max(np.abs(ref)), f"head {h}"
+        assert np.all(Wg[h][ref == 0] == 0), f"head {h}: zero pattern"
+
+
 def test_operator_workload_full_size_sampled_rows(R, oracle_mod):
     """The benchmark's operator workload (B=1 H=8 n=4096 d=64, switches (1,1,0.5), the launch
     it times): sampled rows of every head against the oracle's rows, with the bound and the
@@ -540,6 +557,22 @@ POS_CASES = [
     (1, 4, 1024, 128, "bf16", 1.0, 1.0, 0.5, 1.0),
     (1, 2, 640, 64, "bf16", 0.5, 1.0, 0.5, 0.01),
 ]
+
+
+def test_position_heads_spanning_several_tables(R, oracle_mod):
+    """B=2 H=80 (160 heads, two launch tables) n=300 dv=32 bf16, every output; the same bound
+    as the cases below."""
+    B, H, n, dv = 2, 80, 300, 32
+    pi = W.position_inputs(B, H, n, dv, seed=64, noise=0.5, slope_scale=0.05, beta=1.0, qk=1.0)
+    O = R.position_head(dev(pi.a), dev(pi.v.reshape(B, H, n, dv), torch.bfloat16), 1.0, 1.0)
+    torch.cuda.synchronize()
+    Og = O.cpu().double().numpy().reshape(B * H, n, dv)
+    bq, qq = [f32(x) for x in pi.switches_bh()]
+    ref, st = oracle_mod.position_heads(pi.a, pi.v, bq, qq)
+    absr, _ = oracle_mod.position_heads(pi.a, np.abs(pi.v), bq, qq)
+    assert np.all(st == 0)
+    bound = 2.0 ** -7 * absr + 1e-6 * (1.0 + np.max(absr))
+    assert np.all(np.abs(Og - ref) <= bound)
 
 
 @pytest.mark.parametrize("case", POS_CASES, ids=[str(i) for i in range(len(POS_CASES))])
