@@ -217,6 +217,9 @@ HEAD_CASES = [
     (1, 2, 131, 64, 128, "fp32", 0.7, 1.0, 0.6, (0.7, 1.0), 0.05),
     (1, 1, 1, 64, 64, "bf16", 1.0, 1.0, 0.5, (0.0, 1.0), 0.0),
     (1, 3, 256, 128, 64, "bf16", 1.0, 0.0, 0.5, (0.9, 1.0), 0.0),
+    # head and value widths padded to 128 inside the kernel (partial 64-column regions)
+    (1, 2, 200, 96, 80, "bf16", 1.0, 1.0, 0.5, (0.8, 1.0), 0.0),
+    (1, 2, 333, 120, 72, "bf16", 1.0, 1.0, 0.0, (0.0, 1.0), 0.0),
     # rows of dv % 4 != 0 floats are written by plain stores instead of tensor-map stores
     (1, 2, 200, 64, 5, "bf16", 1.0, 1.0, 0.5, (0.5, 1.0), 0.0),
     (1, 2, 150, 16, 7, "fp32", 0.5, 1.0, 0.0, (0.0, 1.0), 0.0),
