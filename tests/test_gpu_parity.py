@@ -128,7 +128,8 @@ def check_chain(y_gpu, y_ref, env):
     assert np.all(err <= GATE_TOL * env + 1e-30), float(np.max(err / np.maximum(env, 1e-300)))
 
 
-@pytest.mark.parametrize("n,dv", [(1, 16), (130, 16), (300, 64), (1000, 64), (513, 128), (777, 5)])
+@pytest.mark.parametrize("n,dv", [(1, 16), (130, 16), (300, 64), (1000, 64), (513, 128), (777, 5),
+                                  (400, 100), (260, 40)])
 def test_chain_matches_oracle(R, oracle_mod, n, dv):
     B, H = 1, 3
     r = np.random.default_rng(200 + n)
@@ -353,6 +354,8 @@ QK0_CASES = [
     (257, 128, "bf16", 0.25, 0.0, (0.0, 1.0), 0.0),
     (129, 16, "bf16", 0.75, 0.3, (-0.5, 1.5), 0.0),
     (1, 64, "bf16", 1.0, 1.0, (0.0, 1.0), 0.0),
+    (400, 100, "bf16", 1.0, 0.3, (0.5, 1.0), 0.0),
+    (2000, 24, "fp32", 0.6, 0.0, (0.0, 1.0), 0.0),
 ]
 
 
